@@ -1,0 +1,202 @@
+"""Float64 CPU oracle: ctypes binding for ``smc_oracle.c``.
+
+TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline
+leg of ``bench.py`` may import this package. The product path (the CUDA library and its
+Python binding) never imports it, and the two share no code.
+
+Every wrapper takes numpy arrays: bf16 logits as ``uint16`` bit patterns, fp32 logits as
+``float32``. The C functions cite the passages of the pages they follow.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "smc_oracle.c")
+_LIB = os.path.join(_HERE, "libsmc_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+OK, EINVAL, EDTYPE, ENONFINITE, ERANGE = 0, -1, -2, -5, -6
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with the host C compiler (portable flags, no FMA contraction)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+        )
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            P = ctypes.c_void_p
+            i, d, f, ll = ctypes.c_int, ctypes.c_double, ctypes.c_float, ctypes.c_longlong
+            lib.oracle_row_lse.argtypes = [P, i, ll, i, d, P]
+            lib.oracle_sample_inverse_cdf.argtypes = [P, i, d, P, P]
+            lib.oracle_sd_verify.argtypes = [P, P, i, P, P, P, i, i, i, f, P, P, P, P, P, P, P]
+            lib.oracle_smc_reweight.argtypes = [P, P, i, P, i, i, i, f, f, P, P, P, P, P, P, P]
+            lib.oracle_ess_resample.argtypes = [P, i, i, f, P, P, P, P, P, P]
+            lib.oracle_pagetable_remap.argtypes = [P, P, i, i, P, P, i, P, i]
+            lib.oracle_pacer_block_stop.argtypes = [P, P, f, i, i, i, i, f, f, P, P, P]
+            for fn in (lib.oracle_row_lse, lib.oracle_sample_inverse_cdf, lib.oracle_sd_verify,
+                       lib.oracle_smc_reweight, lib.oracle_ess_resample, lib.oracle_pagetable_remap,
+                       lib.oracle_pacer_block_stop):
+                fn.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _dtype_code(logits: np.ndarray) -> int:
+    if logits.dtype == np.float32:
+        return 0
+    if logits.dtype == np.uint16:
+        return 1
+    raise TypeError("logits must be float32 or uint16 (bf16 bits)")
+
+
+class OracleError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: oracle status {code}")
+        self.code = code
+
+
+def _check(rc: int, where: str):
+    if rc != OK:
+        raise OracleError(rc, where)
+
+
+def row_lse(logits: np.ndarray, row: int, V: int, scale: float) -> float:
+    lib = _load()
+    logits = np.ascontiguousarray(logits)
+    out = np.zeros(1, np.float64)
+    _check(lib.oracle_row_lse(_p(logits), _dtype_code(logits), row, V, scale, _p(out)), "row_lse")
+    return float(out[0])
+
+
+def sample_inverse_cdf(r: np.ndarray, u: float):
+    lib = _load()
+    r = np.ascontiguousarray(r, dtype=np.float64)
+    tok = np.zeros(1, np.int32)
+    marg = np.zeros(1, np.float64)
+    _check(lib.oracle_sample_inverse_cdf(_p(r), r.size, float(u), _p(tok), _p(marg)), "inverse_cdf")
+    return int(tok[0]), float(marg[0])
+
+
+def sd_verify(tgt, drf, draft_tokens, S, K, V, temperature, uniforms, tgt_offsets=None,
+              drf_offsets=None, raise_on_error=True):
+    """Returns a dict with accept_len, out_token, lse_tgt, lse_drf, accept_margin,
+    token_margin and status."""
+    lib = _load()
+    tgt = np.ascontiguousarray(tgt)
+    drf = np.ascontiguousarray(drf)
+    dt = _dtype_code(tgt)
+    assert _dtype_code(drf) == dt
+    draft_tokens = np.ascontiguousarray(draft_tokens, dtype=np.int32)
+    uniforms = np.ascontiguousarray(uniforms, dtype=np.float32)
+    to = None if tgt_offsets is None else np.ascontiguousarray(tgt_offsets, dtype=np.int32)
+    do = None if drf_offsets is None else np.ascontiguousarray(drf_offsets, dtype=np.int32)
+    rows_t = tgt.size // V
+    rows_d = max(drf.size // V, 1)
+    out = dict(
+        accept_len=np.full(S, -7, np.int32), out_token=np.full(S, -7, np.int32),
+        lse_tgt=np.full(rows_t, np.nan), lse_drf=np.full(rows_d, np.nan),
+        accept_margin=np.full(max(S * K, 1), -1.0), token_margin=np.full(S, np.nan),
+    )
+    rc = lib.oracle_sd_verify(_p(tgt), _p(drf), dt, _p(draft_tokens), _p(to), _p(do), S, K, V,
+                              float(temperature), _p(uniforms), _p(out["accept_len"]),
+                              _p(out["out_token"]), _p(out["lse_tgt"]), _p(out["lse_drf"]),
+                              _p(out["accept_margin"]), _p(out["token_margin"]))
+    out["status"] = rc
+    if raise_on_error:
+        _check(rc, "sd_verify")
+    return out
+
+
+def smc_reweight(tgt, drf, draft_tokens, S, K, V, temperature, alpha, uniforms, logw,
+                 raise_on_error=True):
+    """``logw`` (float32 [S]) is copied, updated and returned in the dict."""
+    lib = _load()
+    tgt = np.ascontiguousarray(tgt)
+    drf = np.ascontiguousarray(drf)
+    dt = _dtype_code(tgt)
+    draft_tokens = np.ascontiguousarray(draft_tokens, dtype=np.int32)
+    uniforms = np.ascontiguousarray(uniforms, dtype=np.float32)
+    lw = np.array(logw, dtype=np.float32, copy=True)
+    out = dict(
+        logw=lw, bonus_token=np.full(S, -7, np.int32), lse_tgt=np.full(S * (K + 1), np.nan),
+        lse_drf=np.full(max(S * K, 1), np.nan), bonus_margin=np.full(S, np.nan),
+        dlogw=np.full(S, np.nan),
+    )
+    rc = lib.oracle_smc_reweight(_p(tgt), _p(drf), dt, _p(draft_tokens), S, K, V,
+                                 float(temperature), float(alpha), _p(uniforms), _p(lw),
+                                 _p(out["bonus_token"]), _p(out["lse_tgt"]), _p(out["lse_drf"]),
+                                 _p(out["bonus_margin"]), _p(out["dlogw"]))
+    out["status"] = rc
+    if raise_on_error:
+        _check(rc, "smc_reweight")
+    return out
+
+
+def ess_resample(logw, G, N, ess_threshold, uniforms, raise_on_error=True):
+    lib = _load()
+    lw = np.array(logw, dtype=np.float32, copy=True)
+    uniforms = np.ascontiguousarray(uniforms, dtype=np.float32)
+    out = dict(
+        logw=lw, ancestors=np.full(G * N, -7, np.int32), ess=np.full(G, np.nan, np.float32),
+        resampled=np.full(G, -7, np.int32), ess_margin=np.full(G, np.nan),
+        anc_margin=np.full(G * N, np.nan),
+    )
+    rc = lib.oracle_ess_resample(_p(lw), G, N, float(ess_threshold), _p(uniforms),
+                                 _p(out["ancestors"]), _p(out["ess"]), _p(out["resampled"]),
+                                 _p(out["ess_margin"]), _p(out["anc_margin"]))
+    out["status"] = rc
+    if raise_on_error:
+        _check(rc, "ess_resample")
+    return out
+
+
+def pagetable_remap(ancestors, resampled, G, N, table_in, pages_per_seq, num_pages=0,
+                    with_refcount=True, raise_on_error=True):
+    lib = _load()
+    anc = np.ascontiguousarray(ancestors, dtype=np.int32)
+    res = None if resampled is None else np.ascontiguousarray(resampled, dtype=np.int32)
+    tin = np.ascontiguousarray(table_in, dtype=np.int32)
+    tout = np.full(G * N * pages_per_seq, -7, np.int32)
+    rc_arr = np.full(max(num_pages, 1), -7, np.int32) if with_refcount else None
+    rc = lib.oracle_pagetable_remap(_p(anc), _p(res), G, N, _p(tin), _p(tout), pages_per_seq,
+                                    _p(rc_arr), num_pages)
+    if raise_on_error:
+        _check(rc, "pagetable_remap")
+    return dict(table_out=tout, refcount=rc_arr, status=rc)
+
+
+def pacer_block_stop(hidden, w, c, S, b, max_blocks, d, t0, rho, raise_on_error=True):
+    lib = _load()
+    hidden = np.ascontiguousarray(hidden, dtype=np.uint16)
+    w = np.ascontiguousarray(w, dtype=np.uint16)
+    out = dict(lengths=np.full(S, -7, np.int32), block_scores=np.full(S * max_blocks, np.nan),
+               margin=np.full(S, np.nan))
+    rc = lib.oracle_pacer_block_stop(_p(hidden), _p(w), float(c), S, b, max_blocks, d,
+                                     float(t0), float(rho), _p(out["lengths"]),
+                                     _p(out["block_scores"]), _p(out["margin"]))
+    out["status"] = rc
+    if raise_on_error:
+        _check(rc, "pacer_block_stop")
+    return out
