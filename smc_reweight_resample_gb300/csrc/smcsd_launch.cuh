@@ -1,0 +1,106 @@
+// smcsd_launch.cuh -- launch parameters of the kernels and the host-side launchers that the C ABI
+// layer (api.cu) calls.
+#pragma once
+
+#include "smcsd_internal.cuh"
+
+namespace smcsd {
+
+enum StreamMode { kModeSD = 0, kModeSMC = 1, kModeSMCStep = 2 };
+
+// One streaming pass over all logits rows (SD first pass, SMC reweight, fused SMC step).
+struct StreamParams {
+    Rows R;
+    int dtype;
+    bool vec;  // 16-byte aligned rows: vector loads
+    int mode;
+    Scale sc_t, sc_d;
+    Exp2Table T;
+    const float* uniforms;  // SD: [S*(K+1)]; SMC: bonus draws [S]
+    // SD outputs
+    int32_t* accept_len;
+    float* lse_tgt;
+    float* lse_drf;
+    // SMC outputs
+    float* logw;
+    int32_t* bonus_token;
+    // fused SMC step: per-group stage
+    int G, N;
+    float ess_threshold;
+    const float* resample_uniforms;
+    int32_t* ancestors;
+    float* ess;
+    int32_t* resampled;
+    const int32_t* table_in;
+    int32_t* table_out;
+    int pages_per_seq;
+    int32_t* refcount;
+    int num_pages;
+    // scratch
+    void* ws;
+    WsLayout L;
+    int cpr, slots;
+    long long items;
+};
+
+// SD second and third passes (precise sums of the rows to draw from, the residual draw).
+struct SampleParams {
+    Rows R;
+    int dtype;
+    bool vec;
+    Scale sc;
+    Exp2Table T;
+    const float* uniforms;
+    int32_t* out_token;
+    void* ws;
+    WsLayout L;
+    int cpr;
+};
+
+struct ResampleParams {
+    float* logw;
+    int G, N;
+    float ess_threshold;
+    const float* uniforms;
+    int32_t* ancestors;
+    float* ess;
+    int32_t* resampled;
+    void* ws;
+};
+
+struct RemapParams {
+    const int32_t* ancestors;
+    const int32_t* resampled;
+    int G, N;
+    const int32_t* table_in;
+    int32_t* table_out;
+    int pages_per_seq;
+    int32_t* refcount;
+    int num_pages;
+    void* ws;
+};
+
+struct PacerParams {
+    const uint16_t* hidden;
+    const uint16_t* w;
+    float c;
+    int S, b, max_blocks, d;
+    float t0, rho;
+    bool vec;
+    int32_t* lengths;
+    float* block_scores;
+    int32_t* tgt_offsets;
+    int32_t* drf_offsets;
+    void* ws;
+    WsLayout L;
+};
+
+cudaError_t launch_stream(const StreamParams& p, cudaStream_t st);
+cudaError_t launch_sd_sample(const SampleParams& p, cudaStream_t st);
+cudaError_t launch_resample(const ResampleParams& p, cudaStream_t st);
+cudaError_t launch_remap(const RemapParams& p, cudaStream_t st);
+cudaError_t launch_pacer(const PacerParams& p, cudaStream_t st);
+
+int device_sm_count();
+
+}  // namespace smcsd

@@ -19,3 +19,17 @@ def orc():
 
     oracle.build()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def smcsd():
+    """The CUDA library, built in-tree if stale, loaded through its binding (GPU tests only)."""
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from smc_reweight_resample_gb300 import _binding, build
+
+    build.build()
+    _binding.load()
+    return _binding

@@ -1,0 +1,70 @@
+"""The CUDA library builds, loads and exports every entry point that include/smcsd.h declares;
+the host-only entry points and argument checks work without a GPU (nothing is enqueued)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "smcsd.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from smc_reweight_resample_gb300 import build
+
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("sd_verify", "smc_reweight", "smc_ess_resample", "kv_pagetable_remap",
+              "pacer_block_stop", "smc_step", "smcsd_workspace_size", "smcsd_workspace_init",
+              "smcsd_check_status", "smcsd_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_host_only_entry_points(lib):
+    lib.smcsd_status_string.restype = ctypes.c_char_p
+    assert lib.smcsd_status_string(0) == b"ok"
+    assert b"range" in lib.smcsd_status_string(-6)
+    lib.smcsd_workspace_size.restype = ctypes.c_size_t
+    n3 = lib.smcsd_workspace_size(2, 128, 4, 128256)
+    assert n3 > 0 and n3 % 256 == 0
+    assert lib.smcsd_workspace_size(0, 0, 4, 100) == 0
+    assert lib.smcsd_workspace_size(99, 4, 4, 100) == 0
+
+
+def test_argument_checks_return_before_any_cuda_call(lib):
+    P = ctypes.c_void_p
+    lib.sd_verify.argtypes = [P, P, ctypes.c_int, P, P, P, ctypes.c_int, ctypes.c_int,
+                              ctypes.c_int, ctypes.c_float, P, P, P, P, P, P, ctypes.c_size_t, P]
+    fake = P(256)
+    # unsupported dtype
+    assert lib.sd_verify(fake, fake, 7, fake, None, None, 4, 2, 10, 1.0, fake, fake, fake, None,
+                         None, fake, 1 << 20, None) == -2
+    # null target logits
+    assert lib.sd_verify(None, fake, 1, fake, None, None, 4, 2, 10, 1.0, fake, fake, fake, None,
+                         None, fake, 1 << 20, None) == -1
+    # temperature <= 0
+    assert lib.sd_verify(fake, fake, 1, fake, None, None, 4, 2, 10, 0.0, fake, fake, fake, None,
+                         None, fake, 1 << 20, None) == -1
+    # one ragged offset array without the other
+    assert lib.sd_verify(fake, fake, 1, fake, fake, None, 4, 2, 10, 1.0, fake, fake, fake, None,
+                         None, fake, 1 << 20, None) == -1
+    # workspace too small
+    assert lib.sd_verify(fake, fake, 1, fake, None, None, 4, 2, 10, 1.0, fake, fake, fake, None,
+                         None, fake, 16, None) == -3
