@@ -1,0 +1,439 @@
+"""Benchmark: one SMC-SD step per iteration on the Llama-3-vocabulary workload.
+
+Workload (synthetic): 8 prompts x 16 particles, K=4 draft tokens, V=128256, bf16 logits
+(draft ~ N(0,3), target = draft + N(0,1)), T=1, ESS threshold N/2, systematic resampling and
+the page-table remap of a 2048-token context in 16-token pages. One step = smc_step: every
+target and draft logit read once (logsumexp of 1152 rows), the log-weight update, the
+(K+1)-th token of every particle, per-group ESS, resampling and page-table remap.
+
+Timing: W warm-up steps, then exactly K steps on the device, bracketed by a barrier and a
+synchronize, timed with CUDA events on the launching stream. Steps are replayed from a CUDA
+graph that cycles through 4 logit sets of 295.5 MB each (the working set exceeds the 129 MB
+L2, so no step is served from cache). Metric: verified positions/s = S*(K+1) per step.
+
+`--impl reference` times the float64 CPU oracle (single thread) on a bounded sample of the
+same workload and prints the same JSON line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "verified positions/s at V=128256 bf16; achieved HBM GB/s as % of GB300 peak"
+UNIT = "positions/s"
+NSETS = 4
+
+
+def workload_config():
+    from smc_reweight_resample_gb300 import synth
+
+    cfg = synth.SMC_LLAMA3
+    return cfg, {
+        "workload": "smc_sd_step_8x16_k4_v128256_bf16",
+        "G": cfg.G, "N": cfg.N, "K": cfg.K, "V": cfg.V, "temperature": cfg.temperature,
+        "alpha": cfg.alpha, "ess_threshold": cfg.ess_threshold, "ctx": cfg.ctx,
+        "page": cfg.page, "positions_per_step": cfg.S * (cfg.K + 1),
+        "l2": f"inputs larger than L2: {NSETS} rotating logit sets of "
+              f"{logit_bytes(cfg) / 1e6:.1f} MB",
+    }
+
+
+def logit_bytes(cfg) -> int:
+    return cfg.S * (2 * cfg.K + 1) * cfg.V * 2
+
+
+def algorithmic_bytes(cfg) -> int:
+    """Bytes one step must move: every logit once, plus tokens, uniforms, weights and tables."""
+    small = (cfg.S * cfg.K * 4 + cfg.S * 4 + cfg.G * 4 + cfg.S * 4 * 2 + cfg.S * 4 + cfg.G * 8
+             + 2 * cfg.S * cfg.pages_per_seq * 4 + cfg.S * cfg.pages_per_seq * 4)
+    return logit_bytes(cfg) + small
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# --------------------------------------------------------------------------------------------
+# clocks
+# --------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.proc = None
+        self.gpu = gpu_index
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        rows = []
+        for ts, line in self.samples:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((ts, parts))
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        window = "timed region"
+        if len(inside) < 2:  # a short timed region: take the samples around it
+            inside = [r for r in rows if t0 - 1.0 <= r[0] <= t1 + 1.0]
+            window = "timed region +-1 s (region shorter than the 100 ms sampling period)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": "none"}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[1]) for _, p in inside if num(p[1]) is not None]
+        mx = [num(p[2]) for _, p in inside if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, p in inside for i in range(4) if p[5 + i].lower() == "active"})
+        pw = [num(p[3]) for _, p in inside if num(p[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "power_w_max": max(pw) if pw else None, "samples": len(inside), "window": window}
+
+
+# --------------------------------------------------------------------------------------------
+# oracle CPU baseline
+# --------------------------------------------------------------------------------------------
+
+_GROUP_CACHE = {}
+
+
+def _group_inputs(cfg, seed: int):
+    """One prompt group's inputs (N particles), generated once and reused by the timing loop."""
+    key = (cfg.name, seed)
+    if key not in _GROUP_CACHE:
+        from smc_reweight_resample_gb300 import synth
+
+        x = synth.smc_step_inputs(
+            synth.SMCConfig(cfg.name, 1, cfg.N, cfg.K, cfg.V, cfg.sigma_d, cfg.sigma_t,
+                            cfg.temperature, cfg.alpha, cfg.ctx, cfg.page), seed, 0)
+        _GROUP_CACHE[key] = x
+    return _GROUP_CACHE[key]
+
+
+def oracle_positions(cfg, seconds: float, seed: int = 0):
+    """Runs the float64 oracle on whole particles (and their group's ESS, resampling and
+    page-table remap) of the workload for about `seconds` of oracle time, cycling through one
+    pre-generated group of N particles. Returns (positions/s, positions, particles, seconds)."""
+    import numpy as np
+
+    import oracle
+    from smc_reweight_resample_gb300 import synth
+
+    oracle.build()
+    x = _group_inputs(cfg, seed)
+    K, V, N = cfg.K, cfg.V, cfg.N
+    table = synth.initial_page_table(N, cfg.pages_per_seq)
+    t_oracle = 0.0
+    positions = 0
+    particles = 0
+    lw = np.zeros(N, np.float32)
+    while t_oracle < seconds or particles == 0:
+        j = particles % N
+        tgt = x.tgt[j * (K + 1):(j + 1) * (K + 1)]
+        drf = x.drf[j * K:(j + 1) * K]
+        toks = x.draft_tokens[j * K:(j + 1) * K]
+        t0 = time.perf_counter()
+        o = oracle.smc_reweight(tgt, drf, toks, 1, K, V, cfg.temperature, cfg.alpha,
+                                x.bonus_uniforms[j:j + 1], lw[j:j + 1])
+        lw[j] = o["logw"][0]
+        if j == N - 1:
+            r = oracle.ess_resample(lw, 1, N, cfg.ess_threshold, x.resample_uniforms[:1])
+            oracle.pagetable_remap(r["ancestors"], r["resampled"], 1, N, table, cfg.pages_per_seq,
+                                   num_pages=N * cfg.pages_per_seq)
+            lw = r["logw"]
+        t_oracle += time.perf_counter() - t0
+        positions += K + 1
+        particles += 1
+    return positions / t_oracle, positions, particles, t_oracle
+
+
+def cpu_baseline(cfg, seconds=12.0):
+    rate, pos, parts, secs = oracle_positions(cfg, seconds)
+    return {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{parts} particles ({pos} positions, {parts * (2 * cfg.K + 1)} rows of "
+                      f"{cfg.V} bf16 logits) cycling through one group of {cfg.N} particles of the "
+                      f"same workload, with the group's ESS, resampling and remap; {secs:.1f} s "
+                      f"of single-thread float64 oracle time"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    cfg, config = workload_config()
+    budget = 120.0
+    per_step = max(0.02, budget / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_positions(cfg, per_step)
+    rates, times, pos_total = [], [], 0
+    t_all = 0.0
+    for _ in range(args.steps):
+        rate, pos, parts, secs = oracle_positions(cfg, per_step)
+        pos_total += pos
+        t_all += secs
+    value = pos_total / t_all
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * t_all / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config,
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"each step: whole particles of the workload for about "
+                                   f"{per_step:.2f} s of single-thread float64 oracle time "
+                                   f"({pos_total} positions in total)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------------------------
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    cfg, config = workload_config()
+    config["parallelism"] = f"replicas x{world} (independent prompt groups per GPU, no collective)"
+
+    base = None
+    if rank == 0 and not args.no_cpu_baseline:
+        base = cpu_baseline(cfg, args.cpu_seconds)  # before any GPU work
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    from smc_reweight_resample_gb300 import _binding as B
+    from smc_reweight_resample_gb300 import build as _build
+    from smc_reweight_resample_gb300 import synth
+
+    _build.build()
+    B.load()
+    S, K, V, G, N, P = cfg.S, cfg.K, cfg.V, cfg.G, cfg.N, cfg.pages_per_seq
+    dev = torch.device("cuda", local)
+    sets = []
+    for i in range(NSETS):
+        tgt, drf = synth.torch_logits_pair(1000 * rank + i, S, K, V, cfg.sigma_d, cfg.sigma_t, dev)
+        toks = synth.torch_gumbel_draft_tokens(77 + 1000 * rank + i, drf, cfg.temperature)
+        ub = torch.from_numpy(synth.uniforms(rank, S, stream=100 + 2 * i)).to(dev)
+        ur = torch.from_numpy(synth.uniforms(rank, G, stream=101 + 2 * i)).to(dev)
+        sets.append((tgt, drf, toks, ub, ur))
+    torch.cuda.synchronize()
+    ws = B.Workspace(B.OP_SMC_STEP, S, K, V, dev)
+    logw = torch.zeros(S, dtype=torch.float32, device=dev)
+    tables = [torch.from_numpy(synth.initial_page_table(S, P)).to(dev),
+              torch.empty(S * P, dtype=torch.int32, device=dev)]
+    outs = dict(bonus_token=torch.empty(S, dtype=torch.int32, device=dev),
+                ancestors=torch.empty(S, dtype=torch.int32, device=dev),
+                ess=torch.empty(G, dtype=torch.float32, device=dev),
+                resampled=torch.empty(G, dtype=torch.int32, device=dev),
+                refcount=torch.empty(S * P, dtype=torch.int32, device=dev))
+
+    def step(i, stream):
+        tgt, drf, toks, ub, ur = sets[i % NSETS]
+        B.smc_step(tgt, drf, toks, G, N, K, V, cfg.temperature, cfg.alpha, ub, logw,
+                   cfg.ess_threshold, ur, table_in=tables[i % 2], pages_per_seq=P,
+                   num_pages=S * P, ws=ws, table_out=tables[(i + 1) % 2], stream=stream, **outs)
+
+    stream = torch.cuda.Stream(device=dev)
+    # warm-up, eager
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 1)):
+            step(i, stream)
+    stream.synchronize()
+    assert B.check_status(ws, stream) == 0
+    # capture NSETS consecutive steps (an even count keeps the page-table double buffer aligned)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(NSETS):
+            step(i, stream)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    reps, tail = divmod(args.steps, NSETS)
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    clocks = ClockSampler(vis.split(",")[local] if vis else local)
+    clocks.start()
+    time.sleep(0.3)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        for i in range(tail):
+            step(i, stream)
+        ev1.record(stream)
+    ev1.synchronize()
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    time.sleep(0.3)
+    clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    assert B.check_status(ws, stream) == 0
+    ms_per_step = ms / args.steps
+    positions = S * (K + 1)
+    value = world * positions * args.steps / (ms / 1000.0)
+
+    # e2e: inputs from pinned host memory, results back to the host, every step
+    e2e = None
+    if not args.no_e2e:
+        e_steps = min(args.steps, args.e2e_steps)
+        host_sets = []
+        for i in range(2):
+            tgt, drf, toks, ub, ur = sets[i]
+            host_sets.append([x.cpu().pin_memory() for x in (tgt, drf, toks, ub, ur)])
+        dsets = [[torch.empty_like(x) for x in sets[0]] for _ in range(2)]
+        hout = [torch.empty(S, dtype=torch.int32).pin_memory(), torch.empty(S, dtype=torch.int32).pin_memory(),
+                torch.empty(G, dtype=torch.float32).pin_memory(), torch.empty(G, dtype=torch.int32).pin_memory(),
+                torch.empty(S, dtype=torch.float32).pin_memory()]
+        h2d = sum(x.numel() * x.element_size() for x in host_sets[0])
+        d2h = sum(x.numel() * x.element_size() for x in hout)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for i in range(e_steps):
+                hs, ds = host_sets[i % 2], dsets[i % 2]
+                for h, d in zip(hs, ds):
+                    d.copy_(h, non_blocking=True)
+                tgt, drf, toks, ub, ur = ds
+                B.smc_step(tgt, drf, toks, G, N, K, V, cfg.temperature, cfg.alpha, ub, logw,
+                           cfg.ess_threshold, ur, table_in=tables[i % 2], pages_per_seq=P,
+                           num_pages=S * P, ws=ws, table_out=tables[(i + 1) % 2], stream=stream,
+                           **outs)
+                for h, d in zip(hout, (outs["bonus_token"], outs["ancestors"], outs["ess"],
+                                        outs["resampled"], logw)):
+                    h.copy_(d, non_blocking=True)
+        stream.synchronize()
+        t1 = time.perf_counter()
+        et = t1 - t0
+        if world > 1:
+            t = torch.tensor([et], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            et = float(t.item())
+        e2e = {"value": world * positions * e_steps / et, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": e_steps,
+               "note": "pinned host inputs copied to the device, smc_step through the C ABI, "
+                       "results copied back, every step, one stream, no overlap"}
+
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
+    peak, peak_kind = measured_peaks()
+    alg = algorithmic_bytes(cfg)
+    achieved = alg / (ms_per_step / 1000.0) / 1e9
+    traffic = args.ncu_traffic
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "stream_kernel<bf16, fused step> (+ its 64 KB refcount memset)",
+                     "peak_kind": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                     "algorithmic_bytes_per_launch": alg,
+                     "frac_of_8TBps_spec": achieved / 8000.0},
+        "cpu_baseline": base, "e2e": e2e, "gpu_launches": args.steps,
+        "clocks": clocks.summary(t_wall0, t_wall1),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--e2e-steps", type=int, default=40)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ncu-traffic", type=float, default=None,
+                    help="dram bytes per launch of the dominant kernel from an ncu capture")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
