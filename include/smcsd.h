@@ -37,8 +37,9 @@
  *     is enqueued (bad argument, dtype, workspace size) or at launch (CUDA error). Errors that
  *     depend on device data (non-finite logits, token ids or offsets out of range) are recorded
  *     in `ws` and read with smcsd_check_status(). The kernels never trap and never wait on
- *     another block, so a bad input cannot fault or hang the GPU; outputs are unspecified
- *     after such an error.
+ *     another block; the waits inside a block (the copy pipeline of the streaming pass) give
+ *     up after about 2 s and record SMCSD_ERR_TIMEOUT. So a bad input cannot fault or hang the
+ *     GPU; outputs are unspecified after such an error.
  */
 #ifndef SMCSD_H
 #define SMCSD_H
@@ -58,6 +59,7 @@ extern "C" {
 #define SMCSD_ERR_CUDA (-4)        /* a CUDA call or kernel launch failed */
 #define SMCSD_ERR_NONFINITE (-5)   /* device: NaN/+inf logit or weight, or an all-masked row */
 #define SMCSD_ERR_RANGE (-6)       /* device: token id, offset, ancestor or page id out of range */
+#define SMCSD_ERR_TIMEOUT (-7)     /* device: a bounded wait inside a kernel ran out (about 2 s) */
 
 /* logit element types */
 #define SMCSD_F32 0

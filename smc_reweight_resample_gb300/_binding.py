@@ -15,7 +15,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libsmcsd.so")
 
-OK, ERR_INVALID_ARG, ERR_DTYPE, ERR_WORKSPACE, ERR_CUDA, ERR_NONFINITE, ERR_RANGE = 0, -1, -2, -3, -4, -5, -6
+OK, ERR_INVALID_ARG, ERR_DTYPE, ERR_WORKSPACE, ERR_CUDA, ERR_NONFINITE, ERR_RANGE, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5, -6, -7
 F32, BF16 = 0, 1
 OP_SD_VERIFY, OP_SMC_REWEIGHT, OP_SMC_STEP, OP_ESS_RESAMPLE, OP_PAGETABLE_REMAP, OP_PACER_BLOCK_STOP = range(6)
 

@@ -79,6 +79,7 @@ extern "C" const char* smcsd_status_string(int code) {
         case SMCSD_ERR_CUDA: return "CUDA launch or runtime error";
         case SMCSD_ERR_NONFINITE: return "non-finite input (NaN/+inf logit or weight, or an all-masked row)";
         case SMCSD_ERR_RANGE: return "index out of range (token id, offsets, ancestor or page id)";
+        case SMCSD_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out";
         default: return "unknown status";
     }
 }
@@ -105,6 +106,8 @@ extern "C" int sd_verify(const void* tgt_logits, const void* drf_logits, int dty
             ((size_t)V * elem_bytes(dtype)) % 16 == 0;
     p.mode = kModeSD;
     p.sc_t = p.sc_d = make_scale(1.0 / (double)temperature);
+    p.use_table = dtype == SMCSD_BF16 && p.sc_t.c <= kTabMaxScale;
+    p.direct = p.use_table && p.sc_t.c <= kDirectMaxScale;
     p.T = exp2_table();
     p.uniforms = uniforms;
     p.accept_len = accept_len;
@@ -115,6 +118,9 @@ extern "C" int sd_verify(const void* tgt_logits, const void* drf_logits, int dty
     p.cpr = chunks_per_row(V, dtype);
     p.slots = 2 * K + 1;
     p.items = (long long)S * p.slots * p.cpr;
+    if (p.items >= (1ll << 31)) return SMCSD_ERR_INVALID_ARG;
+    p.div_seq = make_fastdiv((uint32_t)(p.slots * p.cpr));
+    p.div_cpr = make_fastdiv((uint32_t)p.cpr);
     cudaError_t e = launch_stream(p, st);
     if (e != cudaSuccess) return SMCSD_ERR_CUDA;
 
@@ -122,6 +128,8 @@ extern "C" int sd_verify(const void* tgt_logits, const void* drf_logits, int dty
     q.R = p.R;
     q.dtype = dtype;
     q.vec = p.vec;
+    q.use_table = p.use_table;
+    q.direct = p.direct;
     q.sc = p.sc_t;
     q.T = p.T;
     q.uniforms = uniforms;
@@ -150,6 +158,8 @@ static int smc_common(const void* tgt_logits, const void* drf_logits, int dtype,
             ((size_t)V * elem_bytes(dtype)) % 16 == 0;
     p.sc_t = make_scale((double)alpha / (double)temperature);
     p.sc_d = make_scale(1.0 / (double)temperature);
+    p.use_table = dtype == SMCSD_BF16 && p.sc_t.c <= kTabMaxScale;
+    p.direct = p.use_table && p.sc_t.c <= kDirectMaxScale;
     p.T = exp2_table();
     p.uniforms = uniforms;
     p.logw = logw;
@@ -159,6 +169,9 @@ static int smc_common(const void* tgt_logits, const void* drf_logits, int dtype,
     p.cpr = chunks_per_row(V, dtype);
     p.slots = 2 * K + 1;
     p.items = (long long)S * p.slots * p.cpr;
+    if (p.items >= (1ll << 31)) return SMCSD_ERR_INVALID_ARG;
+    p.div_seq = make_fastdiv((uint32_t)(p.slots * p.cpr));
+    p.div_cpr = make_fastdiv((uint32_t)p.cpr);
     return SMCSD_OK;
 }
 

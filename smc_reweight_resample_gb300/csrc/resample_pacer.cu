@@ -8,7 +8,6 @@
 //     hidden states only up to the block that stops; the last block to finish writes the ragged
 //     row offsets for the verify that follows.
 #include "smcsd_launch.cuh"
-#include "smcsd_sampling.cuh"
 
 namespace smcsd {
 

@@ -6,36 +6,29 @@
 // Pass 2 (sd_rows_kernel): double-float chunk sums of exp(z/T) over the row(s) to draw from.
 //   Its per-sequence epilogue draws the bonus token directly, or turns the sums into the
 //   reciprocal normalisers 1/Z_t, 1/Z_d that the residual needs.
-// Pass 3 (sd_residual_kernel): double-float chunk sums of max(0, p_i - q_i); its epilogue draws
-//   the correction token (or falls back to p at the same row if the residual has no mass).
+// Pass 3 (sd_residual_kernel): double-float sums of max(0, p_i - q_i) per lane block; its
+//   epilogue draws the correction token (or falls back to p at the same row if the residual
+//   has no mass).
 // Both passes re-read one or two rows per sequence, which the first pass has just streamed.
 #include "smcsd_launch.cuh"
-#include "smcsd_sampling.cuh"
 
 namespace smcsd {
 
-constexpr int kSampleThreads = 256;
+constexpr int kSampleThreads = 512;
 
-__device__ __forceinline__ void load_table_smem2(const Exp2Table& src, Exp2Table& dst) {
-    for (int i = threadIdx.x; i < 32; i += blockDim.x) {
-        dst.hi[i] = src.hi[i];
-        dst.lo[i] = src.lo[i];
-    }
-    __syncthreads();
-}
-
-// residual weight max(0, p_i - q_i) of one logit pair, p_i = exp(c zt) / Z_t etc.
 struct ResidualCtx {
-    Scale sc;
     int n_t, n_d;
     dd inv_t, inv_d;
 };
-__device__ __forceinline__ dd residual_weight(float zt, float zd, const ResidualCtx& c,
-                                              const Exp2Table& T, void* ws) {
-    ddx et, ed;
-    dd pt{0.0f, 0.0f}, qd{0.0f, 0.0f};
-    if (precise_exp(zt, c.sc, T, ws, et)) pt = dd_mul(scaled(et, c.n_t), c.inv_t);
-    if (precise_exp(zd, c.sc, T, ws, ed)) qd = dd_mul(scaled(ed, c.n_d), c.inv_d);
+
+// max(0, p_i - q_i), p_i = exp(c zt) / Z_t, q_i = exp(c zd) / Z_d, from raw logit bits.
+template <int DT>
+__device__ __forceinline__ dd residual_weight(uint32_t bt, uint32_t bd, const ResidualCtx& c,
+                                              const PreciseCtx& P) {
+    dd pt = precise_weight<DT>(bt, c.n_t, P);
+    dd qd = precise_weight<DT>(bd, c.n_d, P);
+    if (pt.hi > 0.0f) pt = dd_mul(pt, c.inv_t);
+    if (qd.hi > 0.0f) qd = dd_mul(qd, c.inv_d);
     dd d = two_sum(pt.hi, -qd.hi);
     d.lo = f_add(d.lo, f_sub(pt.lo, qd.lo));
     d = two_sum(d.hi, d.lo);
@@ -43,32 +36,26 @@ __device__ __forceinline__ dd residual_weight(float zt, float zd, const Residual
 }
 
 template <int DT>
-struct ResidualSlice {
+struct ResidualBlock {
     const void* trow;
     const void* drow;
     int V;
-    bool vec;
     ResidualCtx c;
-    const Exp2Table* T;
-    void* ws;
-    __device__ __forceinline__ void operator()(int chunk, int sub, int lane,
-                                               dd (&w)[Geo<DT>::kPerVec]) const {
-        float xt[Geo<DT>::kPerVec], xd[Geo<DT>::kPerVec];
-        if (vec) {
-            load_slice<DT, true>(trow, V, chunk, sub, lane, xt);
-            load_slice<DT, true>(drow, V, chunk, sub, lane, xd);
-        } else {
-            load_slice<DT, false>(trow, V, chunk, sub, lane, xt);
-            load_slice<DT, false>(drow, V, chunk, sub, lane, xd);
-        }
+    PreciseCtx P;
+    static constexpr int PL = Geo<DT>::kSub / kWarp;
+    __device__ __forceinline__ void operator()(int chunk, int sub, int lane, dd (&w)[PL]) const {
+        const long long e0 = (long long)chunk * Geo<DT>::kChunk + (long long)sub * Geo<DT>::kSub + lane * PL;
 #pragma unroll
-        for (int q = 0; q < Geo<DT>::kPerVec; ++q) w[q] = residual_weight(xt[q], xd[q], c, *T, ws);
+        for (int q = 0; q < PL; ++q) {
+            const long long e = e0 + q;
+            w[q] = e < V ? residual_weight<DT>(logit_bits<DT>(trow, e), logit_bits<DT>(drow, e), c, P)
+                         : dd{0.0f, 0.0f};
+        }
     }
 };
 
-__device__ __forceinline__ ResidualCtx residual_ctx(const SeqState* st, const Scale& sc) {
+__device__ __forceinline__ ResidualCtx residual_ctx(const SeqState* st) {
     ResidualCtx c;
-    c.sc = sc;
     c.n_t = __ldcg(&st->n_t);
     c.n_d = __ldcg(&st->n_d);
     c.inv_t = dd{__ldcg(&st->inv_t_hi), __ldcg(&st->inv_t_lo)};
@@ -76,10 +63,58 @@ __device__ __forceinline__ ResidualCtx residual_ctx(const SeqState* st, const Sc
     return c;
 }
 
+__device__ __forceinline__ void load_exp2_table_s(const Exp2Table& src, Exp2Table& dst) {
+    for (int i = threadIdx.x; i < 32; i += blockDim.x) {
+        dst.hi[i] = src.hi[i];
+        dst.lo[i] = src.lo[i];
+    }
+    __syncthreads();
+}
+
+template <int DT>
+__device__ __noinline__ void sd_rows_epilogue(const SampleParams& p, const PreciseCtx& P, int s,
+                                              int mode, int lane) {
+    const int cpr = p.cpr;
+    SeqState* seq = ws_ptr<SeqState>(p.ws, p.L.seq);
+    const float4* tot_t = ws_ptr<float4>(p.ws, p.L.ddtot) + (size_t)(s * 2) * cpr;
+    const float4* sub_t = ws_ptr<float4>(p.ws, p.L.ddsub) + (size_t)(s * 2) * cpr * kSubs;
+    if (mode == 0) {
+        const float u = __ldg(p.uniforms + (size_t)s * (p.R.K + 1) + p.R.K);
+        const int tok = draw_precise_row<DT>(tot_t, sub_t, cpr,
+                                             row_ptr<DT>(p.R.tgt, __ldcg(&seq[s].trow), p.R.V),
+                                             p.R.V, P, u, lane, nullptr);
+        if (lane == 0) {
+            if (tok < 0) raise_error(p.ws, kErrNonfinite);
+            p.out_token[s] = tok < 0 ? 0 : tok;
+        }
+    } else {
+        const float4* tot_d = tot_t + cpr;
+        const int nt = row_exponent(tot_t, cpr, lane), nd = row_exponent(tot_d, cpr, lane);
+        const dd Rt = row_total(tot_t, cpr, nt, lane), Rd = row_total(tot_d, cpr, nd, lane);
+        if (lane == 0) {
+            if (!(Rt.hi > 0.0f) || !(Rd.hi > 0.0f)) raise_error(p.ws, kErrNonfinite);
+            const dd it_ = dd_recip(Rt), id_ = dd_recip(Rd);
+            seq[s].n_t = nt;
+            seq[s].n_d = nd;
+            seq[s].inv_t_hi = it_.hi;
+            seq[s].inv_t_lo = it_.lo;
+            seq[s].inv_d_hi = id_.hi;
+            seq[s].inv_d_lo = id_.lo;
+        }
+    }
+}
+
 template <int DT>
 __global__ void __launch_bounds__(kSampleThreads) sd_rows_kernel(const __grid_constant__ SampleParams p) {
     __shared__ Exp2Table sT;
-    load_table_smem2(p.T, sT);
+    __shared__ float2 sTab[DT == 1 ? kTabSize : 1];
+    load_exp2_table_s(p.T, sT);
+    PreciseCtx P{p.sc, &sT, nullptr, p.ws, p.direct};
+    if (DT == 1 && p.use_table) {
+        setup_exp_table(sTab, p.sc, &sT, p.ws, ws_ptr<uint32_t>(p.ws, p.L.tab),
+                        ws_ptr<float2>(p.ws, p.L.tab + 16), p.direct, threadIdx.x, blockDim.x, 0);
+        P.tab = sTab;
+    }
     const int lane = threadIdx.x & 31;
     const int wpb = blockDim.x >> 5;
     const int cpr = p.cpr;
@@ -95,44 +130,37 @@ __global__ void __launch_bounds__(kSampleThreads) sd_rows_kernel(const __grid_co
         if (which == 1 && mode == 0) continue;
         const long long row = which == 0 ? __ldcg(&seq[s].trow) : __ldcg(&seq[s].drow);
         const void* rp = row_ptr<DT>(which == 0 ? p.R.tgt : p.R.drf, row, p.R.V);
-        ChunkRegs<DT> r;
-        if (p.vec)
-            load_chunk<DT, true>(rp, p.R.V, chunk, lane, r);
-        else
-            load_chunk<DT, false>(rp, p.R.V, chunk, lane, r);
         float4* tot = ws_ptr<float4>(p.ws, p.L.ddtot) + (size_t)(s * 2 + which) * cpr + chunk;
-        float4* sub = ws_ptr<float4>(p.ws, p.L.ddsub) + ((size_t)(s * 2 + which) * cpr + chunk) * kLoads;
-        precise_partials<DT>(r, p.sc, sT, p.ws, lane, tot, sub);
+        float4* sub = ws_ptr<float4>(p.ws, p.L.ddsub) + ((size_t)(s * 2 + which) * cpr + chunk) * kSubs;
+        precise_partials<DT>(rp, p.R.V, p.vec, chunk, lane, P, tot, sub);
         const unsigned expected = (unsigned)((mode == 1 ? 2 : 1) * cpr);
-        if (!arrive_last(ws_ptr<unsigned>(p.ws, p.L.cnt_seq2) + s, expected, lane)) continue;
+        if (arrive_last(ws_ptr<unsigned>(p.ws, p.L.cnt_seq2) + s, expected, lane))
+            sd_rows_epilogue<DT>(p, P, s, mode, lane);
+    }
+}
 
-        // epilogue of sequence s
+template <int DT>
+__device__ __noinline__ void sd_residual_epilogue(const SampleParams& p, const PreciseCtx& P,
+                                                  const ResidualCtx& c, int s, const void* trp,
+                                                  const void* drp, int lane) {
+    const int cpr = p.cpr;
+    const float4* tot = ws_ptr<float4>(p.ws, p.L.rtot) + (size_t)s * cpr;
+    const float4* sub = ws_ptr<float4>(p.ws, p.L.rsub) + (size_t)s * cpr * kSubs;
+    const float u = __ldg(p.uniforms + (size_t)s * (p.R.K + 1) + p.R.K);
+    const dd R = row_total(tot, cpr, 0, lane);
+    int tok;
+    if (R.hi > 0.0f) {
+        ResidualBlock<DT> fn{trp, drp, p.R.V, c, P};
+        tok = draw_inverse_cdf<ResidualBlock<DT>::PL>(tot, sub, cpr, Geo<DT>::kChunk, Geo<DT>::kSub, u,
+                                                      lane, fn, nullptr);
+    } else {
         const float4* tot_t = ws_ptr<float4>(p.ws, p.L.ddtot) + (size_t)(s * 2) * cpr;
-        const float4* sub_t = ws_ptr<float4>(p.ws, p.L.ddsub) + (size_t)(s * 2) * cpr * kLoads;
-        if (mode == 0) {
-            const float u = __ldg(p.uniforms + (size_t)s * (p.R.K + 1) + p.R.K);
-            const int tok = draw_precise_row<DT>(tot_t, sub_t, cpr,
-                                                 row_ptr<DT>(p.R.tgt, __ldcg(&seq[s].trow), p.R.V),
-                                                 p.R.V, p.vec, p.sc, sT, u, p.ws, lane, nullptr);
-            if (lane == 0) {
-                if (tok < 0) raise_error(p.ws, kErrNonfinite);
-                p.out_token[s] = tok < 0 ? 0 : tok;
-            }
-        } else {
-            const float4* tot_d = tot_t + cpr;
-            const int nt = row_exponent(tot_t, cpr, lane), nd = row_exponent(tot_d, cpr, lane);
-            const dd Rt = row_total(tot_t, cpr, nt, lane), Rd = row_total(tot_d, cpr, nd, lane);
-            if (lane == 0) {
-                if (!(Rt.hi > 0.0f) || !(Rd.hi > 0.0f)) raise_error(p.ws, kErrNonfinite);
-                const dd it_ = dd_recip(Rt), id_ = dd_recip(Rd);
-                seq[s].n_t = nt;
-                seq[s].n_d = nd;
-                seq[s].inv_t_hi = it_.hi;
-                seq[s].inv_t_lo = it_.lo;
-                seq[s].inv_d_hi = id_.hi;
-                seq[s].inv_d_lo = id_.lo;
-            }
-        }
+        const float4* sub_t = ws_ptr<float4>(p.ws, p.L.ddsub) + (size_t)(s * 2) * cpr * kSubs;
+        tok = draw_precise_row<DT>(tot_t, sub_t, cpr, trp, p.R.V, P, u, lane, nullptr);
+    }
+    if (lane == 0) {
+        if (tok < 0) raise_error(p.ws, kErrNonfinite);
+        p.out_token[s] = tok < 0 ? 0 : tok;
     }
 }
 
@@ -140,8 +168,15 @@ template <int DT>
 __global__ void __launch_bounds__(kSampleThreads)
     sd_residual_kernel(const __grid_constant__ SampleParams p) {
     __shared__ Exp2Table sT;
-    load_table_smem2(p.T, sT);
-    constexpr int PV = Geo<DT>::kPerVec;
+    __shared__ float2 sTab[DT == 1 ? kTabSize : 1];
+    load_exp2_table_s(p.T, sT);
+    PreciseCtx P{p.sc, &sT, nullptr, p.ws, p.direct};
+    if (DT == 1 && p.use_table) {
+        setup_exp_table(sTab, p.sc, &sT, p.ws, ws_ptr<uint32_t>(p.ws, p.L.tab),
+                        ws_ptr<float2>(p.ws, p.L.tab + 16), p.direct, threadIdx.x, blockDim.x, 0);
+        P.tab = sTab;
+    }
+    constexpr int SUB = Geo<DT>::kSub;
     const int lane = threadIdx.x & 31;
     const int wpb = blockDim.x >> 5;
     const int cpr = p.cpr;
@@ -153,53 +188,30 @@ __global__ void __launch_bounds__(kSampleThreads)
         const int chunk = (int)(it - (long long)s * cpr);
         if (seq_len(p.R, s, p.ws) < 0) continue;
         if (__ldcg(&seq[s].mode) != 1) continue;
-        const long long tr = __ldcg(&seq[s].trow), dr = __ldcg(&seq[s].drow);
-        const void* trp = row_ptr<DT>(p.R.tgt, tr, p.R.V);
-        const void* drp = row_ptr<DT>(p.R.drf, dr, p.R.V);
-        const ResidualCtx c = residual_ctx(seq + s, p.sc);
-        dd total{0.0f, 0.0f};
-        float4 mine = make_float4(0.f, 0.f, 0.f, 0.f);
+        const void* trp = row_ptr<DT>(p.R.tgt, __ldcg(&seq[s].trow), p.R.V);
+        const void* drp = row_ptr<DT>(p.R.drf, __ldcg(&seq[s].drow), p.R.V);
+        const ResidualCtx c = residual_ctx(seq + s);
+        // this lane's block of SUB logits, processed in quarters
+        const long long e0 = (long long)chunk * Geo<DT>::kChunk + (long long)lane * SUB;
+        dd acc{kBias, 0.0f};
 #pragma unroll 1
-        for (int v = 0; v < kLoads; ++v) {
-            float xt[PV], xd[PV];
-            if (p.vec) {
-                load_slice<DT, true>(trp, p.R.V, chunk, v, lane, xt);
-                load_slice<DT, true>(drp, p.R.V, chunk, v, lane, xd);
-            } else {
-                load_slice<DT, false>(trp, p.R.V, chunk, v, lane, xt);
-                load_slice<DT, false>(drp, p.R.V, chunk, v, lane, xd);
-            }
-            dd acc{kBias, 0.0f};
+        for (int q0 = 0; q0 < SUB; q0 += 16) {
 #pragma unroll
-            for (int q = 0; q < PV; ++q) acc_biased(acc, residual_weight(xt[q], xd[q], c, sT, p.ws));
-            const dd sv = warp_sum_dd(unbias(acc));
-            total = dd_add(total, sv);
-            if (lane == v) mine = pack_part(sv, 0);
+            for (int q = 0; q < 16; ++q) {
+                const long long e = e0 + q0 + q;
+                if (e < p.R.V)
+                    acc_biased(acc, residual_weight<DT>(logit_bits<DT>(trp, e), logit_bits<DT>(drp, e), c, P));
+            }
+            acc = fast_two_sum(acc.hi, acc.lo);
         }
+        const dd sv = unbias(acc);
         float4* tot = ws_ptr<float4>(p.ws, p.L.rtot) + (size_t)s * cpr;
-        float4* sub = ws_ptr<float4>(p.ws, p.L.rsub) + (size_t)s * cpr * kLoads;
-        if (lane < kLoads) sub[(size_t)chunk * kLoads + lane] = mine;
+        float4* sub = ws_ptr<float4>(p.ws, p.L.rsub) + (size_t)s * cpr * kSubs;
+        sub[(size_t)chunk * kSubs + lane] = pack_part(sv, 0);
+        const dd total = warp_sum_dd(sv);
         if (lane == 0) tot[chunk] = pack_part(total, 0);
-        if (!arrive_last(ws_ptr<unsigned>(p.ws, p.L.cnt_seq3) + s, (unsigned)cpr, lane)) continue;
-
-        // epilogue: draw from the residual, or from p at the same row if it has no mass
-        const float u = __ldg(p.uniforms + (size_t)s * (p.R.K + 1) + p.R.K);
-        const dd R = row_total(tot, cpr, 0, lane);
-        int tok;
-        if (R.hi > 0.0f) {
-            ResidualSlice<DT> fn{trp, drp, p.R.V, p.vec, c, &sT, p.ws};
-            tok = draw_inverse_cdf<PV>(tot, sub, cpr, Geo<DT>::kChunk, Geo<DT>::kSub, u, lane, fn,
-                                       nullptr);
-        } else {
-            const float4* tot_t = ws_ptr<float4>(p.ws, p.L.ddtot) + (size_t)(s * 2) * cpr;
-            const float4* sub_t = ws_ptr<float4>(p.ws, p.L.ddsub) + (size_t)(s * 2) * cpr * kLoads;
-            tok = draw_precise_row<DT>(tot_t, sub_t, cpr, trp, p.R.V, p.vec, p.sc, sT, u, p.ws, lane,
-                                       nullptr);
-        }
-        if (lane == 0) {
-            if (tok < 0) raise_error(p.ws, kErrNonfinite);
-            p.out_token[s] = tok < 0 ? 0 : tok;
-        }
+        if (arrive_last(ws_ptr<unsigned>(p.ws, p.L.cnt_seq3) + s, (unsigned)cpr, lane))
+            sd_residual_epilogue<DT>(p, P, c, s, trp, drp, lane);
     }
 }
 
@@ -209,9 +221,9 @@ static int grid_for(Kern kern, long long warps_needed) {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kSampleThreads, 0) != cudaSuccess)
         occ = 1;
     const int wpb = kSampleThreads / kWarp;
-    long long want = (warps_needed + wpb - 1) / wpb;
-    long long cap = (long long)device_sm_count() * (occ > 0 ? occ : 1);
-    long long g = want < cap ? want : cap;
+    const long long want = (warps_needed + wpb - 1) / wpb;
+    const long long cap = (long long)device_sm_count() * (occ > 0 ? occ : 1);
+    const long long g = want < cap ? want : cap;
     return (int)(g < 1 ? 1 : g);
 }
 

@@ -2,7 +2,7 @@
 // layer (api.cu) calls.
 #pragma once
 
-#include "smcsd_internal.cuh"
+#include "smcsd_sampling.cuh"
 
 namespace smcsd {
 
@@ -12,7 +12,9 @@ enum StreamMode { kModeSD = 0, kModeSMC = 1, kModeSMCStep = 2 };
 struct StreamParams {
     Rows R;
     int dtype;
-    bool vec;  // 16-byte aligned rows: vector loads
+    bool vec;        // 16-byte aligned rows: vector loads
+    bool use_table;  // bf16 exp table for the sampled rows
+    bool direct;     // the table holds exp(c z) itself
     int mode;
     Scale sc_t, sc_d;
     Exp2Table T;
@@ -40,7 +42,9 @@ struct StreamParams {
     void* ws;
     WsLayout L;
     int cpr, slots;
-    long long items;
+    long long items;       // chunks in the sequence-major order (< 2^31)
+    FastDiv div_seq;       // by slots * cpr (chunks per sequence)
+    FastDiv div_cpr;       // by cpr (chunks per row)
 };
 
 // SD second and third passes (precise sums of the rows to draw from, the residual draw).
@@ -48,6 +52,8 @@ struct SampleParams {
     Rows R;
     int dtype;
     bool vec;
+    bool use_table;
+    bool direct;
     Scale sc;
     Exp2Table T;
     const float* uniforms;
@@ -95,7 +101,8 @@ struct PacerParams {
     WsLayout L;
 };
 
-cudaError_t launch_stream(const StreamParams& p, cudaStream_t st);
+cudaError_t launch_stream(const StreamParams& p, cudaStream_t st);      // dispatch
+cudaError_t launch_stream_tma(const StreamParams& p, cudaStream_t st);  // aligned rows
 cudaError_t launch_sd_sample(const SampleParams& p, cudaStream_t st);
 cudaError_t launch_resample(const ResampleParams& p, cudaStream_t st);
 cudaError_t launch_remap(const RemapParams& p, cudaStream_t st);

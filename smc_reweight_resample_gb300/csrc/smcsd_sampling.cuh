@@ -1,7 +1,9 @@
-// smcsd_sampling.cuh -- per-chunk partials, row normalisers, the inverse-CDF draw over a row,
-// and per-group effective sample size with systematic resampling. Warp-level device code
-// shared by the kernels.
+// smcsd_sampling.cuh -- chunk partials (fast and precise), row normalisers, the inverse-CDF
+// draw over a row, and per-group effective sample size with systematic resampling. Warp-level
+// device code shared by the kernels.
 #pragma once
+
+#include <cuda_bf16.h>
 
 #include "smcsd_internal.cuh"
 
@@ -13,90 +15,457 @@ __device__ __forceinline__ float hw_exp2(float x) {
     return y;
 }
 
+// floor(t) as an int for |t| < 2^22: add 1.5 * 2^23 rounding toward -inf, read the low bits.
+__device__ __forceinline__ int floor_int(float t) {
+    return __float_as_int(__fadd_rd(t, 12582912.0f)) - 0x4B400000;
+}
+
+// Scale c = alpha / T as a double-float (from the double quotient), c * log2(e) as float, and
+// c in double for the normalisers.
+struct Scale {
+    float c_hi, c_lo;
+    float c2;
+    double c;
+};
+
+// ------------------------------------------------------------------------------------------
+// precise weights exp(c z) of sampled rows
+// ------------------------------------------------------------------------------------------
+//
+// exp(c z) is represented as e * 2^n with n = floor(z * c2) computed in float and e (about
+// [1, 2)) a double-float. For bf16 logits with 2^-12 <= |z| < 64, e comes from a table over all
+// such bf16 values (4608 entries, filled per block from the general routine below, so both give
+// identical bits); other logits use the general routine (double-float exp_split).
+
+constexpr uint32_t kTabMagLo = 0x3980u;        // bf16 bits of 2^-12
+constexpr uint32_t kTabMagHi = 0x4280u;        // bf16 bits of 64
+constexpr uint32_t kTabHalf = kTabMagHi - kTabMagLo;  // entries per sign
+constexpr int kTabSize = 2 * (int)kTabHalf;    // 4608
+// the table is used only while |64 * c2| stays far inside floor_int's range
+constexpr double kTabMaxScale = 4096.0;
+
+struct PreciseCtx {
+    Scale sc;
+    const Exp2Table* T;  // shared memory
+    const float2* tab;   // shared memory, or nullptr (float32 logits / very large scale)
+    void* ws;
+    bool direct;         // tab holds exp(c z) itself (c small enough to stay in float range)
+};
+
+// With c * 64 * log2(e) <= 125 every table value exp(c z), |z| < 64, is a normal float, so the
+// table can hold the double-float value itself; then a logit's weight relative to 2^nref is one
+// table load and two multiplies. Chunks whose largest weight is below 2^-60 use the general
+// routine instead (their low words would be subnormal).
+constexpr double kDirectMaxScale = 1.35;
+constexpr int kDirectMinRef = -60;
+
+struct GW {
+    float x, y;
+    int n;
+    int ok;
+};
+
+// exp(c z) = (x + y) * 2^n for any float z; ok = 0 for a weight of zero (-inf, or c z below
+// -kMaxScaledLogit). NaN, +inf or c z above kMaxScaledLogit raise SMCSD_ERR_NONFINITE.
+static __device__ __noinline__ GW general_weight(float z, float c_hi, float c_lo, float c2,
+                                          const Exp2Table* T, void* ws) {
+    GW r{0.0f, 0.0f, 0, 0};
+    if (!(z > kNegInf)) {
+        if (z != z) raise_error(ws, kErrNonfinite);
+        return r;
+    }
+    const dd x = dd_mul_f(dd{c_hi, c_lo}, z);
+    if (!(x.hi <= kMaxScaledLogit)) {
+        raise_error(ws, kErrNonfinite);
+        return r;
+    }
+    if (x.hi < -kMaxScaledLogit) return r;
+    const ddx e = exp_split(x, *T);
+    r.n = floor_int(f_mul(z, c2));
+    const float s = pow2i(e.n - r.n);
+    r.x = f_mul(e.hi, s);
+    r.y = f_mul(e.lo, s);
+    r.ok = 1;
+    return r;
+}
+
+__device__ __forceinline__ void bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Fill a table (threads tid = 0..nthr-1 take part, then barrier `bar` over nthr threads).
+__device__ __forceinline__ void build_exp_table(float2* tab, const Scale& sc, const Exp2Table* T,
+                                                void* ws, bool direct, int tid, int nthr, int bar) {
+    for (int i = tid; i < kTabSize; i += nthr) {
+        const uint32_t mag = kTabMagLo + (uint32_t)(i % (int)kTabHalf);
+        const uint32_t b = mag | (i >= (int)kTabHalf ? 0x8000u : 0u);
+        const GW g = general_weight(__uint_as_float(b << 16), sc.c_hi, sc.c_lo, sc.c2, T, ws);
+        if (direct) {
+            const float t = pow2i(g.n);
+            tab[i] = make_float2(f_mul(g.x, t), f_mul(g.y, t));
+        } else {
+            tab[i] = make_float2(g.x, g.y);
+        }
+    }
+    bar_sync(bar, nthr);
+}
+
+// The block's shared-memory table for scale sc. The first block that builds it for a workspace
+// publishes it there (tag words: magic, then c_hi, c_lo, c2 bits); later calls with the same
+// scale copy it instead of rebuilding. A published table is never overwritten, so a reader can
+// never see a half-written one; calls with another scale build their own copy each time.
+constexpr uint32_t kTabMagic = 0x54424c32u;
+__device__ __forceinline__ void setup_exp_table(float2* tab, const Scale& sc, const Exp2Table* T,
+                                                void* ws, uint32_t* gtag, float2* gtab, bool direct,
+                                                int tid, int nthr, int bar) {
+    __shared__ int state;  // 0: build and publish, 1: copy, 2: build only
+    if (tid == 0) {
+        uint32_t magic;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(magic) : "l"(gtag) : "memory");
+        if (magic != kTabMagic)
+            state = blockIdx.x == 0 ? 0 : 2;
+        else
+            state = (__ldcg(gtag + 1) == __float_as_uint(sc.c_hi) &&
+                     __ldcg(gtag + 2) == __float_as_uint(sc.c_lo) &&
+                     __ldcg(gtag + 3) == __float_as_uint(sc.c2))
+                        ? 1
+                        : 2;
+    }
+    bar_sync(bar, nthr);
+    const int st = state;
+    if (st == 1) {
+        const uint4* src = reinterpret_cast<const uint4*>(gtab);
+        uint4* dst = reinterpret_cast<uint4*>(tab);
+        for (int i = tid; i < kTabSize / 2; i += nthr) dst[i] = __ldcg(src + i);
+        bar_sync(bar, nthr);
+        return;
+    }
+    build_exp_table(tab, sc, T, ws, direct, tid, nthr, bar);
+    if (st == 0) {
+        const uint4* src = reinterpret_cast<const uint4*>(tab);
+        uint4* dst = reinterpret_cast<uint4*>(gtab);
+        for (int i = tid; i < kTabSize / 2; i += nthr) dst[i] = src[i];
+        __threadfence();
+        bar_sync(bar, nthr);
+        if (tid == 0) {
+            gtag[1] = __float_as_uint(sc.c_hi);
+            gtag[2] = __float_as_uint(sc.c_lo);
+            gtag[3] = __float_as_uint(sc.c2);
+            __threadfence();
+            asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(gtag), "r"(kTabMagic) : "memory");
+        }
+    }
+}
+
+// Weight exp(c z) / 2^nref of one logit given its raw bits (see logit_bits), as a double-float.
+template <int DT>
+__device__ __forceinline__ dd precise_weight(uint32_t b, int nref, const PreciseCtx& P) {
+    float ex, ey;
+    int n;
+    if (DT == 1 && P.tab && (!P.direct || nref >= kDirectMinRef)) {
+        const uint32_t off = (b & 0x7fffu) - kTabMagLo;
+        if (off < kTabHalf) {
+            const float2 e = P.tab[off + ((b & 0x8000u) ? kTabHalf : 0u)];
+            ex = e.x;
+            ey = e.y;
+            n = P.direct ? 0 : floor_int(f_mul(bits_to_float<DT>(b), P.sc.c2));
+        } else {
+            const GW g = general_weight(bits_to_float<DT>(b), P.sc.c_hi, P.sc.c_lo, P.sc.c2, P.T, P.ws);
+            if (!g.ok) return dd{0.0f, 0.0f};
+            ex = g.x;
+            ey = g.y;
+            n = g.n;
+        }
+    } else {
+        const GW g = general_weight(bits_to_float<DT>(b), P.sc.c_hi, P.sc.c_lo, P.sc.c2, P.T, P.ws);
+        if (!g.ok) return dd{0.0f, 0.0f};
+        ex = g.x;
+        ey = g.y;
+        n = g.n;
+    }
+    const float s = pow2i(n - nref);
+    return dd{f_mul(ex, s), f_mul(ey, s)};
+}
+
+// Accumulate y (0 <= y <= ~2) into a biased accumulator whose high part stays >= 4, so that
+// Dekker's fast-two-sum is exact.
+constexpr float kBias = 4.0f;
+__device__ __forceinline__ void acc_biased(dd& acc, dd y) {
+    const float s = f_add(acc.hi, y.hi);
+    const float err = f_sub(y.hi, f_sub(s, acc.hi));
+    acc.lo = f_add(acc.lo, f_add(err, y.lo));
+    acc.hi = s;
+}
+__device__ __forceinline__ dd unbias(dd acc) { return fast_two_sum(f_sub(acc.hi, kBias), acc.lo); }
+
+// Partial record of a sampled row: value = (x + y) * 2^n (z holds n's bits).
+__device__ __forceinline__ float4 pack_part(dd v, int n) {
+    return make_float4(v.hi, v.lo, __int_as_float(n), 0.0f);
+}
+constexpr int kNoMass = INT_MIN / 2;  // n of a chunk without mass
+
+// ------------------------------------------------------------------------------------------
+// chunk loads
+// ------------------------------------------------------------------------------------------
+
+// Interleaved chunk load for the fast path: vector v of lane l holds logits
+// chunk*kChunk + v*(kChunk/8) + l*kPerVec + [0, kPerVec). Logits beyond V read as -inf.
+template <int DT>
+__device__ __forceinline__ void load_chunk_interleaved(const void* row, int V, bool vec, int chunk,
+                                                       int lane, uint4 (&raw)[kLoads]) {
+    constexpr int PV = Geo<DT>::kPerVec;
+    const long long base = (long long)chunk * Geo<DT>::kChunk + lane * PV;
+    if (vec) {
+#pragma unroll
+        for (int v = 0; v < kLoads; ++v) {
+            const long long e = base + v * (Geo<DT>::kChunk / kLoads);
+            raw[v] = e < V ? ld_stream16(static_cast<const char*>(row) + e * Geo<DT>::kBytes)
+                           : (DT == 0 ? make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u)
+                                      : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u));
+        }
+    } else {
+#pragma unroll
+        for (int v = 0; v < kLoads; ++v) {
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (DT == 0) {
+                    const long long e = base + v * (Geo<DT>::kChunk / kLoads) + j;
+                    w[j] = e < V ? logit_bits<0>(row, e) : 0xff800000u;
+                } else {
+                    const long long e = base + v * (Geo<DT>::kChunk / kLoads) + 2 * j;
+                    const uint32_t lo = e < V ? logit_bits<1>(row, e) : 0xff80u;
+                    const uint32_t hi = e + 1 < V ? logit_bits<1>(row, e + 1) : 0xff80u;
+                    w[j] = lo | (hi << 16);
+                }
+            }
+            raw[v] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+}
+
+// A lane's contiguous block of kSub logits of a chunk (128 bytes) as 32 raw words; logits
+// beyond V read as -inf.
+template <int DT>
+__device__ __forceinline__ void load_lane_block(const void* row, int V, bool vec, int chunk,
+                                                int lane, uint32_t (&w)[32]) {
+    constexpr int SUB = Geo<DT>::kSub;
+    const long long e0 = (long long)chunk * Geo<DT>::kChunk + (long long)lane * SUB;
+    if (vec && e0 + SUB <= V) {
+        const uint4* p = reinterpret_cast<const uint4*>(static_cast<const char*>(row) + e0 * Geo<DT>::kBytes);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint4 q = __ldcg(p + i);
+            w[4 * i] = q.x;
+            w[4 * i + 1] = q.y;
+            w[4 * i + 2] = q.z;
+            w[4 * i + 3] = q.w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            if (DT == 0) {
+                w[j] = e0 + j < V ? logit_bits<0>(row, e0 + j) : 0xff800000u;
+            } else {
+                const uint32_t lo = e0 + 2 * j < V ? logit_bits<1>(row, e0 + 2 * j) : 0xff80u;
+                const uint32_t hi = e0 + 2 * j + 1 < V ? logit_bits<1>(row, e0 + 2 * j + 1) : 0xff80u;
+                w[j] = lo | (hi << 16);
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------------------------------------
 // chunk partials
 // ------------------------------------------------------------------------------------------
 
-// Fast partial of one chunk: {m, sum exp(c (z - m))} with m the chunk's largest logit (raw,
-// before scaling; c > 0 keeps the order). An all-masked chunk gives {-inf, 0}.
+// Fast partial of one chunk: {m, sum_i 2^(z_i c2 - fl(m c2))} with m the chunk's largest logit
+// (raw, before scaling; c > 0 keeps the order). An all-masked chunk gives {-inf, 0}.
 template <int DT>
-__device__ __forceinline__ float2 fast_partial(const ChunkRegs<DT>& r, float c2, void* ws) {
-    constexpr int PV = Geo<DT>::kPerVec;
-    float m = kNegInf;
+__device__ __forceinline__ float2 fast_partial(const uint4 (&raw)[kLoads], float c2, void* ws) {
+    float m;
+    if (DT == 1) {
+        __nv_bfloat162 mx = *reinterpret_cast<const __nv_bfloat162*>(&raw[0].x);
 #pragma unroll
-    for (int v = 0; v < kLoads; ++v)
+        for (int v = 0; v < kLoads; ++v) {
+            const uint32_t w[4] = {raw[v].x, raw[v].y, raw[v].z, raw[v].w};
 #pragma unroll
-        for (int q = 0; q < PV; ++q) m = fmaxf(m, r.x[v][q]);
+            for (int j = 0; j < 4; ++j) mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&w[j]));
+        }
+        const uint32_t mw = *reinterpret_cast<const uint32_t*>(&mx);
+        m = fmaxf(bf16_lo(mw), bf16_hi(mw));
+    } else {
+        m = kNegInf;
+#pragma unroll
+        for (int v = 0; v < kLoads; ++v)
+            m = fmaxf(fmaxf(m, fmaxf(__uint_as_float(raw[v].x), __uint_as_float(raw[v].y))),
+                      fmaxf(__uint_as_float(raw[v].z), __uint_as_float(raw[v].w)));
+    }
     m = warp_max(m);
     if (m == kNegInf) {
         bool nan = false;
 #pragma unroll
-        for (int v = 0; v < kLoads; ++v)
+        for (int v = 0; v < kLoads; ++v) {
+            const uint32_t w[4] = {raw[v].x, raw[v].y, raw[v].z, raw[v].w};
 #pragma unroll
-            for (int q = 0; q < PV; ++q) nan |= (r.x[v][q] != r.x[v][q]);
+            for (int j = 0; j < 4; ++j) {
+                if (DT == 1)
+                    nan |= (bf16_lo(w[j]) != bf16_lo(w[j])) | (bf16_hi(w[j]) != bf16_hi(w[j]));
+                else
+                    nan |= (__uint_as_float(w[j]) != __uint_as_float(w[j]));
+            }
+        }
         if (__any_sync(0xffffffffu, nan) && (threadIdx.x & 31) == 0) raise_error(ws, kErrNonfinite);
         return make_float2(kNegInf, 0.0f);
     }
-    float acc[kLoads];
+    const float nmc2 = -(m * c2);
+    float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
 #pragma unroll
     for (int v = 0; v < kLoads; ++v) {
-        float a = 0.0f;
-#pragma unroll
-        for (int q = 0; q < PV; ++q) a += hw_exp2((r.x[v][q] - m) * c2);
-        acc[v] = a;
+        const uint32_t w[4] = {raw[v].x, raw[v].y, raw[v].z, raw[v].w};
+        if (DT == 1) {
+            a0 += hw_exp2(fmaf(bf16_lo(w[0]), c2, nmc2)) + hw_exp2(fmaf(bf16_hi(w[0]), c2, nmc2));
+            a1 += hw_exp2(fmaf(bf16_lo(w[1]), c2, nmc2)) + hw_exp2(fmaf(bf16_hi(w[1]), c2, nmc2));
+            a2 += hw_exp2(fmaf(bf16_lo(w[2]), c2, nmc2)) + hw_exp2(fmaf(bf16_hi(w[2]), c2, nmc2));
+            a3 += hw_exp2(fmaf(bf16_lo(w[3]), c2, nmc2)) + hw_exp2(fmaf(bf16_hi(w[3]), c2, nmc2));
+        } else {
+            a0 += hw_exp2(fmaf(__uint_as_float(w[0]), c2, nmc2));
+            a1 += hw_exp2(fmaf(__uint_as_float(w[1]), c2, nmc2));
+            a2 += hw_exp2(fmaf(__uint_as_float(w[2]), c2, nmc2));
+            a3 += hw_exp2(fmaf(__uint_as_float(w[3]), c2, nmc2));
+        }
     }
-    float s = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-    s = warp_sum(s);
-    if (!(s == s) || m == -kNegInf) {  // NaN or +inf in the chunk
+    float s = warp_sum((a0 + a1) + (a2 + a3));
+    if (!(s == s) || m == kPosInf) {  // NaN or +inf in the chunk
         if ((threadIdx.x & 31) == 0) raise_error(ws, kErrNonfinite);
     }
     return make_float2(m, s);
 }
 
-// Precise partials of one chunk of a row that will be sampled: eight double-float sums
-// sum_i exp(c z_i) / 2^nref over the 512-byte slices, and their total. Lane v < 8 stores slice
-// v, lane 0 the total.
-template <int DT>
-__device__ __forceinline__ void precise_partials(const ChunkRegs<DT>& r, const Scale& sc,
-                                                 const Exp2Table& T, void* ws, int lane,
-                                                 float4* tot_out, float4* sub_out) {
-    constexpr int PV = Geo<DT>::kPerVec;
+// Precise partials of one chunk of a row that will be sampled. Lane l stores the double-float
+// sum of exp(c z) / 2^nref over its block of kSub logits in sub_out[l]; lane 0 stores the chunk
+// total in *tot_out. nref = floor(m c2) for the chunk's largest logit m. The lane's block comes
+// from `src`: src.vec(i), i = 0..7, returns its eight 16-byte pieces in some order (only valid
+// when the block lies entirely below V, `full`), src.bits(q) the raw bits of its q-th logit.
+template <int DT, typename Src>
+__device__ __forceinline__ void precise_core(const Src& src, bool full, long long e0, int V,
+                                             int lane, const PreciseCtx& P, float4* tot_out,
+                                             float4* sub_out) {
+    constexpr int SUB = Geo<DT>::kSub;
+    // the block's largest logit
     float m = kNegInf;
+    bool nan = false;
+    if (full) {
 #pragma unroll
-    for (int v = 0; v < kLoads; ++v)
+        for (int i = 0; i < 8; ++i) {
+            const uint4 q = src.vec(i);
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-        for (int q = 0; q < PV; ++q) m = fmaxf(m, r.x[v][q]);
+            for (int j = 0; j < 4; ++j) {
+                if (DT == 1) {
+                    const float a = bf16_lo(w[j]), b = bf16_hi(w[j]);
+                    m = fmaxf(m, fmaxf(a, b));
+                    nan |= (a != a) | (b != b);
+                } else {
+                    const float a = __uint_as_float(w[j]);
+                    m = fmaxf(m, a);
+                    nan |= (a != a);
+                }
+            }
+        }
+    } else {
+#pragma unroll 1
+        for (int q = 0; q < SUB; ++q) {
+            if (e0 + q >= V) break;
+            const float a = bits_to_float<DT>(src.bits(q));
+            m = fmaxf(m, a);
+            nan |= (a != a);
+        }
+    }
     m = warp_max(m);
-    ddx em;
-    bool any = m > kNegInf && precise_exp(m, sc, T, ws, em);
-    if (!any) {
-        bool nan = false;
-#pragma unroll
-        for (int v = 0; v < kLoads; ++v)
-#pragma unroll
-            for (int q = 0; q < PV; ++q) nan |= (r.x[v][q] != r.x[v][q]);
-        if (__any_sync(0xffffffffu, nan) && lane == 0) raise_error(ws, kErrNonfinite);
-        if (lane < kLoads) sub_out[lane] = pack_part(dd{0.0f, 0.0f}, kNoMass);
+    nan = __any_sync(0xffffffffu, nan);
+    const float cm = m * (float)P.sc.c;
+    const bool ok = !nan && m > kNegInf && cm >= -kMaxScaledLogit && cm <= kMaxScaledLogit;
+    if (!ok) {
+        // NaN anywhere, +inf, or a scaled logit above the supported range is an error; a chunk
+        // of -inf (or of logits whose weights all vanish) just has no mass
+        const bool too_big = m > kNegInf && !(cm <= kMaxScaledLogit);  // includes +inf
+        if ((nan || too_big) && lane == 0) raise_error(P.ws, kErrNonfinite);
+        sub_out[lane] = pack_part(dd{0.0f, 0.0f}, kNoMass);
         if (lane == 0) *tot_out = pack_part(dd{0.0f, 0.0f}, kNoMass);
         return;
     }
-    const int nref = em.n;
-    float4 mine = make_float4(0.f, 0.f, 0.f, 0.f);
-    dd total{0.0f, 0.0f};
+    const int nref = floor_int(f_mul(m, P.sc.c2));
+    dd acc{kBias, 0.0f};
+    bool rare = false;  // logits outside the table's domain, added in a second pass below
+    const bool direct = DT == 1 && P.tab && P.direct && nref >= kDirectMinRef;
+    const bool general_tab = DT == 1 && P.tab && !P.direct;
+    if (full && (direct || general_tab)) {
+        const float S = pow2i(-nref);
+#pragma unroll 1
+        for (int i = 0; i < 8; ++i) {
+            const uint4 q = src.vec(i);
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-    for (int v = 0; v < kLoads; ++v) {
-        dd acc{kBias, 0.0f};
-#pragma unroll
-        for (int q = 0; q < PV; ++q) {
-            ddx e;
-            if (precise_exp(r.x[v][q], sc, T, ws, e)) acc_biased(acc, scaled(e, nref));
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t b = (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xffffu);
+                const uint32_t off = (b & 0x7fffu) - kTabMagLo;
+                if (off < kTabHalf) {
+                    const float2 e = P.tab[off + ((b & 0x8000u) ? kTabHalf : 0u)];
+                    if (direct) {
+                        acc_biased(acc, dd{f_mul(e.x, S), f_mul(e.y, S)});
+                    } else {
+                        const int n = floor_int(f_mul(bits_to_float<1>(b), P.sc.c2));
+                        const float sc = pow2i(n - nref);
+                        acc_biased(acc, dd{f_mul(e.x, sc), f_mul(e.y, sc)});
+                    }
+                } else {
+                    rare = true;
+                }
+            }
+            acc = fast_two_sum(acc.hi, acc.lo);  // keep the low word small
         }
-        dd sv = warp_sum_dd(unbias(acc));
-        total = dd_add(total, sv);
-        if (lane == v) mine = pack_part(sv, nref);
+    } else {
+        rare = true;
     }
-    if (lane < kLoads) sub_out[lane] = mine;
+    if (__any_sync(0xffffffffu, rare) && rare) {
+        // second pass over this lane's block for the logits the table pass did not cover
+        const bool covered = full && (direct || general_tab);
+#pragma unroll 1
+        for (int q = 0; q < SUB; ++q) {
+            if (e0 + q >= V) break;
+            const uint32_t b = src.bits(q);
+            if (covered && ((b & 0x7fffu) - kTabMagLo) < kTabHalf) continue;
+            acc_biased(acc, precise_weight<DT>(b, nref, P));
+            if ((q & 7) == 7) acc = fast_two_sum(acc.hi, acc.lo);
+        }
+    }
+    const dd sv = unbias(acc);
+    sub_out[lane] = pack_part(sv, nref);
+    const dd total = warp_sum_dd(sv);
     if (lane == 0) *tot_out = pack_part(total, nref);
+}
+
+// Lane block read from global memory (cached in L1 for the second pass).
+template <int DT>
+struct GlobalBlock {
+    const uint4* blk;
+    const void* row;
+    long long e0;
+    __device__ __forceinline__ uint4 vec(int i) const { return __ldca(blk + i); }
+    __device__ __forceinline__ uint32_t bits(int q) const { return logit_bits<DT>(row, e0 + q); }
+};
+
+template <int DT>
+__device__ __forceinline__ void precise_partials(const void* row, int V, bool vec, int chunk,
+                                                 int lane, const PreciseCtx& P, float4* tot_out,
+                                                 float4* sub_out) {
+    constexpr int SUB = Geo<DT>::kSub;
+    const long long e0 = (long long)chunk * Geo<DT>::kChunk + (long long)lane * SUB;
+    const GlobalBlock<DT> src{reinterpret_cast<const uint4*>(static_cast<const char*>(row) +
+                                                             e0 * Geo<DT>::kBytes),
+                              row, e0};
+    precise_core<DT>(src, vec && e0 + SUB <= V, e0, V, lane, P, tot_out, sub_out);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -104,16 +473,17 @@ __device__ __forceinline__ void precise_partials(const ChunkRegs<DT>& r, const S
 // ------------------------------------------------------------------------------------------
 
 // Natural-log normalisers log sum_i exp(c z_i) of up to four rows whose fast partials start at
-// part[r * stride] (cpr chunks each), written to out[r] (r < nrows) on every lane. The four
-// rows' partial loads are in flight together. A row without mass gives NaN.
-__device__ __forceinline__ void rows_lse_fast4(const float2* part, int stride, int nrows, int cpr,
-                                               const Scale& sc, int lane, double (&out)[4]) {
+// part[r * stride] (cpr chunks each). Returns, on lane r < nrows, the normaliser of row r (NaN
+// for a row without mass); the four rows' partial loads are in flight together.
+__device__ __forceinline__ double rows_lse_fast4(const float2* part, int stride, int nrows, int cpr,
+                                                 const Scale& sc, int lane) {
     constexpr int RB = 4;
-    float m[RB], s[RB];
+    float mq[RB], s[RB], M[RB];  // running fl(m c2) of the lane's largest chunk, its sum, max m
 #pragma unroll
     for (int b = 0; b < RB; ++b) {
-        m[b] = kNegInf;
+        mq[b] = kNegInf;
         s[b] = 0.0f;
+        M[b] = kNegInf;
     }
     for (int c0 = 0; c0 < cpr; c0 += 4 * kWarp) {
         float2 v[RB][4];
@@ -121,7 +491,7 @@ __device__ __forceinline__ void rows_lse_fast4(const float2* part, int stride, i
         for (int b = 0; b < RB; ++b)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                int c = c0 + lane + j * kWarp;
+                const int c = c0 + lane + j * kWarp;
                 v[b][j] = (b < nrows && c < cpr) ? ld_cg2(part + (size_t)b * stride + c)
                                                  : make_float2(kNegInf, 0.0f);
             }
@@ -129,28 +499,31 @@ __device__ __forceinline__ void rows_lse_fast4(const float2* part, int stride, i
         for (int b = 0; b < RB; ++b)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                float pm = v[b][j].x, ps = v[b][j].y;
+                const float pm = v[b][j].x, ps = v[b][j].y;
                 if (pm == kNegInf) continue;
-                if (pm > m[b]) {
-                    s[b] = s[b] * hw_exp2((m[b] - pm) * sc.c2) + ps;
-                    m[b] = pm;
+                M[b] = fmaxf(M[b], pm);
+                const float q = pm * sc.c2;
+                if (q > mq[b]) {
+                    s[b] = s[b] * hw_exp2(mq[b] - q) + ps;
+                    mq[b] = q;
                 } else {
-                    s[b] += ps * hw_exp2((pm - m[b]) * sc.c2);
+                    s[b] += ps * hw_exp2(q - mq[b]);
                 }
             }
     }
+    double out = __longlong_as_double(0x7ff8000000000000ll);
 #pragma unroll
     for (int b = 0; b < RB; ++b) {
-        float M = warp_max(m[b]);
-        float t = (m[b] == kNegInf) ? 0.0f : s[b] * hw_exp2((m[b] - M) * sc.c2);
-        float S = warp_sum(t);
-        out[b] = (M == kNegInf || !(S > 0.0f)) ? __longlong_as_double(0x7ff8000000000000ll)
-                                               : sc.c * (double)M + log((double)S);
+        const float Mb = warp_max(M[b]);
+        const float Q = Mb * sc.c2;
+        const float t = (mq[b] == kNegInf) ? 0.0f : s[b] * hw_exp2(mq[b] - Q);
+        const float Ssum = warp_sum(t);
+        if (lane == b && Mb != kNegInf && Ssum > 0.0f) {
+            const float rQ = fmaf(Mb, sc.c2, -Q);  // exact residual of fl(M c2)
+            out = sc.c * (double)Mb + log((double)Ssum) - (double)rQ * 0.69314718055994530942;
+        }
     }
-}
-
-__device__ __forceinline__ double pick4(const double (&a)[4], int i) {
-    return i == 0 ? a[0] : (i == 1 ? a[1] : (i == 2 ? a[2] : a[3]));
+    return out;
 }
 
 // ------------------------------------------------------------------------------------------
@@ -158,25 +531,24 @@ __device__ __forceinline__ double pick4(const double (&a)[4], int i) {
 // ------------------------------------------------------------------------------------------
 
 __device__ __forceinline__ dd part_value(float4 p, int N) {
-    int n = __float_as_int(p.z);
+    const int n = __float_as_int(p.z);
     if (n == kNoMass || !(p.x > 0.0f)) return dd{0.0f, 0.0f};
-    float s = pow2i(n - N);
+    const float s = pow2i(n - N);
     return dd{f_mul(p.x, s), f_mul(p.y, s)};
 }
 
 // Draw token = min{ i : sum_{j<=i} w_j > u * sum_j w_j } over a row whose chunk totals `tot`
-// [cpr] and slice partials `sub` [cpr * 8] were produced by precise_partials (or by the
-// residual pass), rescanning one slice with `slice_weights(chunk, sub, lane, w[PV])`, which
-// must reproduce the per-logit weights in units of 2^N exactly. Returns the token on every
-// lane (-1 if the row has no mass). If `lse` is given it receives log(sum_j w_j) + N ln 2.
-template <int PV, typename SliceFn>
+// [cpr] and lane-block partials `sub` [cpr * kSubs] describe the weights, rescanning one lane
+// block with `block_weights(chunk, sub, lane, w[PL])` (PL = kSub / 32 weights per lane, in
+// units of 2^N, reproducing the partials exactly). Returns the token on every lane (-1 if the
+// row has no mass). If `lse` is given it receives log(sum_j w_j) + N ln 2.
+template <int PL, typename BlockFn>
 __device__ int draw_inverse_cdf(const float4* tot, const float4* sub, int cpr, int chunk_elems,
-                                int sub_elems, float u, int lane, SliceFn slice_weights,
+                                int sub_elems, float u, int lane, BlockFn block_weights,
                                 double* lse) {
-    // common exponent
     int N = kNoMass;
     for (int c = lane; c < cpr; c += kWarp) {
-        float4 t = ld_cg4(tot + c);
+        const float4 t = ld_cg4(tot + c);
         if (t.x > 0.0f) N = max(N, __float_as_int(t.z));
     }
     N = warp_max_i(N);
@@ -187,9 +559,9 @@ __device__ int draw_inverse_cdf(const float4* tot, const float4* sub, int cpr, i
     const int c_begin = min(lane * cpl, cpr), c_end = min(c_begin + cpl, cpr);
     dd loc{0.0f, 0.0f};
     for (int c = c_begin; c < c_end; ++c) loc = dd_add(loc, part_value(ld_cg4(tot + c), N));
-    dd excl = warp_exclusive_scan_dd(loc, lane);
-    dd incl = dd_add(excl, loc);
-    dd R{__shfl_sync(0xffffffffu, incl.hi, 31), __shfl_sync(0xffffffffu, incl.lo, 31)};
+    const dd excl = warp_exclusive_scan_dd(loc, lane);
+    const dd incl = dd_add(excl, loc);
+    const dd R{__shfl_sync(0xffffffffu, incl.hi, 31), __shfl_sync(0xffffffffu, incl.lo, 31)};
     if (lse) *lse = log(dd_to_double(R)) + (double)N * 0.69314718055994530942;
     const dd target = dd_mul_f(R, u);
 
@@ -199,7 +571,7 @@ __device__ int draw_inverse_cdf(const float4* tot, const float4* sub, int cpr, i
     if (bal) {
         owner = __ffs(bal) - 1;
     } else {  // rounding put the target at or past the total: last lane with mass
-        unsigned m = __ballot_sync(0xffffffffu, loc.hi > 0.0f);
+        const unsigned m = __ballot_sync(0xffffffffu, loc.hi > 0.0f);
         owner = 31 - __clz(m);
     }
     int c_star = -1;
@@ -209,11 +581,11 @@ __device__ int draw_inverse_cdf(const float4* tot, const float4* sub, int cpr, i
         int last_pos = -1;
         dd last_base = p;
         for (int c = c_begin; c < c_end; ++c) {
-            dd v = part_value(ld_cg4(tot + c), N);
+            const dd v = part_value(ld_cg4(tot + c), N);
             if (v.hi > 0.0f) {
                 last_pos = c;
                 last_base = p;
-                dd q = dd_add(p, v);
+                const dd q = dd_add(p, v);
                 if (dd_gt(q, target)) {
                     c_star = c;
                     base = p;
@@ -231,34 +603,32 @@ __device__ int draw_inverse_cdf(const float4* tot, const float4* sub, int cpr, i
     base.hi = __shfl_sync(0xffffffffu, base.hi, owner);
     base.lo = __shfl_sync(0xffffffffu, base.lo, owner);
 
-    // slice level
-    dd sv = lane < kLoads ? part_value(ld_cg4(sub + (size_t)c_star * kLoads + lane), N) : dd{0.0f, 0.0f};
-    dd sex = warp_exclusive_scan_dd(sv, lane);
-    dd sin_ = dd_add(dd_add(base, sex), sv);
-    has = sv.hi > 0.0f && dd_gt(sin_, target);
+    // lane-block level: one block per lane
+    const dd sv = part_value(ld_cg4(sub + (size_t)c_star * kSubs + lane), N);
+    const dd sex = warp_exclusive_scan_dd(sv, lane);
+    const dd sbase_l = dd_add(base, sex);
+    has = sv.hi > 0.0f && dd_gt(dd_add(sbase_l, sv), target);
     bal = __ballot_sync(0xffffffffu, has);
     int s_star;
     if (bal) {
         s_star = __ffs(bal) - 1;
     } else {
-        unsigned m = __ballot_sync(0xffffffffu, sv.hi > 0.0f);
+        const unsigned m = __ballot_sync(0xffffffffu, sv.hi > 0.0f);
         s_star = m ? 31 - __clz(m) : 0;
     }
-    dd sbase = dd_add(base, sex);
-    sbase.hi = __shfl_sync(0xffffffffu, sbase.hi, s_star);
-    sbase.lo = __shfl_sync(0xffffffffu, sbase.lo, s_star);
+    dd sbase{__shfl_sync(0xffffffffu, sbase_l.hi, s_star), __shfl_sync(0xffffffffu, sbase_l.lo, s_star)};
 
-    // logit level: rescan the slice
-    dd w[PV];
-    slice_weights(c_star, s_star, lane, w);
+    // logit level: rescan the block (lane l holds logits l*PL .. l*PL+PL-1 of it)
+    dd w[PL];
+    block_weights(c_star, s_star, lane, w);
     dd lsum{0.0f, 0.0f};
 #pragma unroll
-    for (int q = 0; q < PV; ++q) lsum = dd_add(lsum, w[q]);
-    dd lex = warp_exclusive_scan_dd(lsum, lane);
+    for (int q = 0; q < PL; ++q) lsum = dd_add(lsum, w[q]);
+    const dd lex = warp_exclusive_scan_dd(lsum, lane);
     dd p = dd_add(sbase, lex);
     int found = -1, lastpos = -1;
 #pragma unroll
-    for (int q = 0; q < PV; ++q) {
+    for (int q = 0; q < PL; ++q) {
         if (w[q].hi > 0.0f) {
             p = dd_add(p, w[q]);
             lastpos = q;
@@ -271,35 +641,30 @@ __device__ int draw_inverse_cdf(const float4* tot, const float4* sub, int cpr, i
         tok_lane = __ffs(bal) - 1;
         tok_q = __shfl_sync(0xffffffffu, found, tok_lane);
     } else {
-        unsigned m = __ballot_sync(0xffffffffu, lastpos >= 0);
+        const unsigned m = __ballot_sync(0xffffffffu, lastpos >= 0);
         if (!m) return -1;
         tok_lane = 31 - __clz(m);
         tok_q = __shfl_sync(0xffffffffu, lastpos, tok_lane);
     }
-    return c_star * chunk_elems + s_star * sub_elems + tok_lane * PV + tok_q;
+    return c_star * chunk_elems + s_star * sub_elems + tok_lane * PL + tok_q;
 }
 
-// Weights exp(c z) / 2^N of one slice of a row (the rescan for draws from a precise row).
+// Weights exp(c z) / 2^N of one lane block of a row (the rescan of a precise row).
 template <int DT>
-struct PreciseSlice {
+struct PreciseBlock {
     const void* row;
     int V;
-    bool vec;
     int N;
-    Scale sc;
-    const Exp2Table* T;
-    void* ws;
-    __device__ __forceinline__ void operator()(int chunk, int sub, int lane,
-                                               dd (&w)[Geo<DT>::kPerVec]) const {
-        float x[Geo<DT>::kPerVec];
-        if (vec)
-            load_slice<DT, true>(row, V, chunk, sub, lane, x);
-        else
-            load_slice<DT, false>(row, V, chunk, sub, lane, x);
+    PreciseCtx P;
+    static constexpr int PL = Geo<DT>::kSub / kWarp;
+    __device__ __forceinline__ void operator()(int chunk, int sub, int lane, dd (&w)[PL]) const {
+        const long long e0 = (long long)chunk * Geo<DT>::kChunk + (long long)sub * Geo<DT>::kSub + lane * PL;
 #pragma unroll
-        for (int q = 0; q < Geo<DT>::kPerVec; ++q) {
-            ddx e;
-            w[q] = precise_exp(x[q], sc, *T, ws, e) ? scaled(e, N) : dd{0.0f, 0.0f};
+        for (int q = 0; q < PL; ++q) {
+            const long long e = e0 + q;
+            w[q] = (e < V && check_ok(P.ws, e >= 0, -121, e))
+                       ? precise_weight<DT>(logit_bits<DT>(row, e), N, P)
+                       : dd{0.0f, 0.0f};
         }
     }
 };
@@ -308,7 +673,7 @@ struct PreciseSlice {
 __device__ __forceinline__ int row_exponent(const float4* tot, int cpr, int lane) {
     int N = kNoMass;
     for (int c = lane; c < cpr; c += kWarp) {
-        float4 t = ld_cg4(tot + c);
+        const float4 t = ld_cg4(tot + c);
         if (t.x > 0.0f) N = max(N, __float_as_int(t.z));
     }
     return warp_max_i(N);
@@ -323,12 +688,11 @@ __device__ __forceinline__ dd row_total(const float4* tot, int cpr, int N, int l
 
 template <int DT>
 __device__ __forceinline__ int draw_precise_row(const float4* tot, const float4* sub, int cpr,
-                                                const void* row, int V, bool vec, const Scale& sc,
-                                                const Exp2Table& T, float u, void* ws, int lane,
-                                                double* lse) {
-    PreciseSlice<DT> fn{row, V, vec, row_exponent(tot, cpr, lane), sc, &T, ws};
-    return draw_inverse_cdf<Geo<DT>::kPerVec>(tot, sub, cpr, Geo<DT>::kChunk, Geo<DT>::kSub, u,
-                                              lane, fn, lse);
+                                                const void* row, int V, const PreciseCtx& P,
+                                                float u, int lane, double* lse) {
+    PreciseBlock<DT> fn{row, V, row_exponent(tot, cpr, lane), P};
+    return draw_inverse_cdf<PreciseBlock<DT>::PL>(tot, sub, cpr, Geo<DT>::kChunk, Geo<DT>::kSub,
+                                                  u, lane, fn, lse);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -338,7 +702,7 @@ __device__ __forceinline__ int draw_precise_row(const float4* tot, const float4*
 // Number of children j in [0, N) with (j + U) / N < C, with the comparison evaluated exactly as
 // written (double), so that it agrees with the definition a_j = min{ i : C_i > v_j }.
 __device__ __forceinline__ int children_below(double C, double U, int N) {
-    double est = floor(C * (double)N - U);
+    const double est = floor(C * (double)N - U);
     long long j = (long long)est;
     if (j < -1) j = -1;
     if (j > N - 1) j = N - 1;
@@ -349,14 +713,13 @@ __device__ __forceinline__ int children_below(double C, double U, int N) {
 
 // logw [N] of one group (float, in/out). Writes ancestors [N], *ess_out, *res_out (if given).
 // Returns whether the group was resampled (on every lane).
-__device__ __forceinline__ bool group_resample(float* logw, int N, float thr, float U,
-                                               int32_t* anc, float* ess_out, int32_t* res_out,
-                                               void* ws, int lane) {
+static __device__ __noinline__ bool group_resample(float* logw, int N, float thr, float U, int32_t* anc,
+                                            float* ess_out, int32_t* res_out, void* ws, int lane) {
     double M = -__builtin_huge_val();
     bool bad = false;
     for (int i = lane; i < N; i += kWarp) {
-        float v = __ldcg(logw + i);
-        if (v != v || v == -kNegInf) bad = true;
+        const float v = __ldcg(logw + i);
+        if (v != v || v == kPosInf) bad = true;
         M = fmax(M, (double)v);
     }
     M = warp_max_d(M);
@@ -369,7 +732,7 @@ __device__ __forceinline__ bool group_resample(float* logw, int N, float thr, fl
     }
     double W = 0.0, W2 = 0.0;
     for (int i = lane; i < N; i += kWarp) {
-        double w = exp((double)__ldcg(logw + i) - M);
+        const double w = exp((double)__ldcg(logw + i) - M);
         W += w;
         W2 += w * w;
     }
@@ -391,25 +754,23 @@ __device__ __forceinline__ bool group_resample(float* logw, int N, float thr, fl
     const int i0 = min(lane * per, N), i1 = min(i0 + per, N);
     double loc = 0.0;
     for (int i = i0; i < i1; ++i) loc += exp((double)__ldcg(logw + i) - M);
-    double run = warp_exclusive_scan_d(loc, lane);
+    const double run = warp_exclusive_scan_d(loc, lane);
     const double Ud = (double)U;
-    int Jlast = 0;
-    // J at the end of each lane's block, then the previous lane's value as this lane's start
+    int Jend = -1;
     {
         double r = run;
         int J = 0;
         for (int i = i0; i < i1; ++i) {
             r += exp((double)__ldcg(logw + i) - M);
-            double C = (i == N - 1) ? 1.0 : r / W;
+            const double C = (i == N - 1) ? 1.0 : r / W;
             J = children_below(C, Ud, N);
         }
-        Jlast = (i1 > i0) ? J : -1;
+        if (i1 > i0) Jend = J;
     }
-    // propagate: a lane with an empty block passes its predecessor's value on
-    int Jend = Jlast;
+    // a lane with an empty block passes its predecessor's value on
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        int t = __shfl_up_sync(0xffffffffu, Jend, o);
+        const int t = __shfl_up_sync(0xffffffffu, Jend, o);
         if (lane >= o && Jend < 0) Jend = t;
     }
     int Jstart = __shfl_up_sync(0xffffffffu, Jend, 1);
@@ -418,8 +779,8 @@ __device__ __forceinline__ bool group_resample(float* logw, int N, float thr, fl
     int Jprev = Jstart;
     for (int i = i0; i < i1; ++i) {
         r += exp((double)__ldcg(logw + i) - M);
-        double C = (i == N - 1) ? 1.0 : r / W;
-        int J = children_below(C, Ud, N);
+        const double C = (i == N - 1) ? 1.0 : r / W;
+        const int J = children_below(C, Ud, N);
         for (int j = Jprev; j < J; ++j) anc[j] = i;
         Jprev = max(Jprev, J);
     }

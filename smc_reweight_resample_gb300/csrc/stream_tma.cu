@@ -1,0 +1,276 @@
+// stream_tma.cu -- the streaming pass over 16-byte-aligned logits rows as a TMA pipeline.
+//
+// One block per SM: a producer warp whose lane 0 moves 4 KB chunks of logits from HBM into a
+// ring of kRing shared-memory slots with the bulk-copy engine (cp.async.bulk, completion counted
+// on one mbarrier per slot), and kTmaConsumers consumer warps that take the block's chunks in
+// order from a shared counter, wait for their slot, compute the chunk's partial (fast or
+// precise, smcsd_sampling.cuh) from shared memory, hand the slot back (a second mbarrier per
+// slot) and count the chunk for its sequence; the last chunk of a sequence runs its epilogue
+// (smcsd_epilogue.cuh). The producer runs up to kRing chunks (96 KB) ahead, so the consumers
+// never wait on HBM latency, and every logit still crosses HBM exactly once.
+//
+// Chunks are dealt to blocks round-robin (block b owns chunks b, b+B, b+2B, ... of the
+// sequence-major order), so all blocks see the same mix of fast and precise chunks and advance
+// through the sequences together.
+//
+// Every wait is bounded (about 2 s of wall time): a wait that runs out records
+// SMCSD_ERR_TIMEOUT in the workspace and the warp leaves; the producer, before it leaves,
+// waits (again bounded) for the copies it started.
+#include "smcsd_epilogue.cuh"
+
+namespace smcsd {
+
+constexpr int kTmaConsumers = 16;
+constexpr int kTmaThreads = (kTmaConsumers + 1) * kWarp;
+constexpr int kRing = 24;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+constexpr size_t kSmemRing = (size_t)kRing * kChunkBytes;
+constexpr size_t kSmemTab = (size_t)kTabSize * sizeof(float2);
+constexpr size_t kSmemBytes = kSmemRing + kSmemTab + sizeof(Exp2Table) + 2 * kRing * 8 + kRing * 4 + 16;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Wait for the phase of `parity` to complete, for at most kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    return true;
+}
+// Slot tags: the producer writes the index k of the chunk it is about to load into a slot before
+// it arms the slot's barrier. A consumer holding chunk k waits for the tag first, so that the
+// barrier it then waits on is known to be in the phase of chunk k: a parity wait alone cannot
+// tell that phase from the one two loads earlier, and the consumers take chunks from a shared
+// counter, so a consumer can reach a slot before the previous chunk of that slot has landed.
+__device__ __forceinline__ void tag_store(uint32_t addr, uint32_t k) {
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(addr), "r"(k) : "memory");
+}
+__device__ __forceinline__ uint32_t tag_load(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+// Wait (at most kWaitLimitNs) until the tag at `addr` reads k.
+__device__ __forceinline__ bool tag_wait(uint32_t addr, uint32_t k) {
+    if (tag_load(addr) == k) return true;
+    const unsigned long long t0 = global_ns();
+    while (tag_load(addr) != k)
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    return true;
+}
+
+// 1-D bulk copy global -> shared, completion counted in bytes on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// Lane block of a precise chunk from its shared-memory slot. The 16-byte pieces are read with an
+// XOR swizzle (piece i of lane l at (i ^ (l & 7)) * 16) so that each quarter-warp touches eight
+// different bank groups.
+template <int DT>
+struct SmemBlock {
+    const unsigned char* base;  // this lane's 128 bytes
+    int sw;
+    __device__ __forceinline__ uint4 vec(int i) const {
+        return *reinterpret_cast<const uint4*>(base + ((i ^ sw) << 4));
+    }
+    __device__ __forceinline__ uint32_t bits(int q) const {
+        return DT == 1 ? (uint32_t)reinterpret_cast<const unsigned short*>(base)[q]
+                       : reinterpret_cast<const uint32_t*>(base)[q];
+    }
+};
+
+// The producer (one thread) issues the block's chunks in order, each into slot k % kRing once
+// the consumer of that slot's previous chunk has handed it back, tagging the slot with k first.
+template <int DT>
+__device__ __noinline__ void tma_producer(const StreamParams& p, unsigned char* ring,
+                                          uint64_t* full, uint64_t* empty, uint32_t* tag) {
+    const uint32_t B = gridDim.x;
+    const long long row_bytes = (long long)p.R.V * Geo<DT>::kBytes;
+    uint32_t k = 0;
+    for (;; ++k) {
+        const long long it = (long long)blockIdx.x + (long long)k * B;
+        if (it >= p.items) break;
+        const int slot = (int)(k % kRing);
+        const uint32_t round = k / kRing;
+        if (round > 0 && !mbar_wait(smem_u32(&empty[slot]), (round - 1) & 1u)) {
+            raise_error(p.ws, kErrTimeout);
+            break;
+        }
+        const ChunkRef c = chunk_ref(p, (uint32_t)it);
+        const uint32_t fb = smem_u32(&full[slot]);
+        tag_store(smem_u32(&tag[slot]), k);
+        const long long off = (long long)c.chunk * kChunkBytes;
+        const long long left = row_bytes - off;
+        const uint32_t bytes = (uint32_t)(left < kChunkBytes ? left : kChunkBytes);
+        const char* src = static_cast<const char*>(c.is_draft ? p.R.drf : p.R.tgt) +
+                          c.row * row_bytes + off;
+        const uint32_t dst = smem_u32(ring + (size_t)slot * kChunkBytes);
+        const long long nrows = (long long)p.R.S * (c.is_draft ? p.R.K : p.R.K + 1);
+        const bool sane = !c.valid ||
+                          (check_ok(p.ws, c.s >= 0 && c.s < p.R.S, -101, it) &&
+                           check_ok(p.ws, p.R.toff || (c.row >= 0 && c.row < nrows), -102, c.row) &&
+                           check_ok(p.ws, left > 0 && (bytes & 15u) == 0, -103, left) &&
+                           check_ok(p.ws, ((uintptr_t)src & 15u) == 0 && (dst & 15u) == 0, -104,
+                                    (long long)(uintptr_t)src));
+        if (c.valid && sane) {
+            mbar_arrive_expect_tx(fb, bytes);
+            bulk_load(dst, src, bytes, fb);
+        } else {
+            mbar_arrive(fb);
+        }
+    }
+    // the copies of the last kRing chunks may still be in flight: wait for them before leaving
+    const uint32_t first = k > (uint32_t)kRing ? k - kRing : 0u;
+    for (uint32_t j = first; j < k; ++j) mbar_wait(smem_u32(&full[j % kRing]), (j / kRing) & 1u);
+}
+
+template <int DT, int MODE>
+__global__ void __launch_bounds__(kTmaThreads, 1)
+    stream_tma_kernel(const __grid_constant__ StreamParams p) {
+    constexpr bool kPrecise = MODE != kModeSD;
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char* ring = smem;
+    float2* sTab = reinterpret_cast<float2*>(smem + kSmemRing);
+    Exp2Table* sT = reinterpret_cast<Exp2Table*>(smem + kSmemRing + kSmemTab);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSmemRing + kSmemTab + sizeof(Exp2Table));
+    uint64_t* empty = full + kRing;
+    uint32_t* tag = reinterpret_cast<uint32_t*>(empty + kRing);
+    unsigned* next = tag + kRing;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kRing; ++i) {
+            mbar_init(smem_u32(&full[i]), 1);
+            mbar_init(smem_u32(&empty[i]), 1);
+            tag[i] = 0xffffffffu;
+        }
+        *next = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (warp == 0) {
+        if (lane == 0) tma_producer<DT>(p, ring, full, empty, tag);
+        return;
+    }
+
+    // consumers: tables first (while the producer already streams), then chunks
+    const int tid = threadIdx.x - kWarp, nthr = kTmaConsumers * kWarp;
+    for (int i = tid; i < 32; i += nthr) {
+        sT->hi[i] = p.T.hi[i];
+        sT->lo[i] = p.T.lo[i];
+    }
+    bar_sync(1, nthr);
+    PreciseCtx P{p.sc_t, sT, nullptr, p.ws, p.direct};
+    if (kPrecise && DT == 1 && p.use_table) {
+        setup_exp_table(sTab, p.sc_t, sT, p.ws, ws_ptr<uint32_t>(p.ws, p.L.tab),
+                        ws_ptr<float2>(p.ws, p.L.tab + 16), p.direct, tid, nthr, 1);
+        P.tab = sTab;
+    }
+    const long long B = gridDim.x;
+    for (;;) {
+        unsigned k = 0;
+        if (lane == 0) k = atomicAdd(next, 1u);
+        k = __shfl_sync(0xffffffffu, k, 0);
+        const long long it = (long long)blockIdx.x + (long long)k * B;
+        if (it >= p.items) break;
+        const int slot = (int)(k % kRing);
+        const bool ok = tag_wait(smem_u32(&tag[slot]), k) && mbar_wait(smem_u32(&full[slot]), (k / kRing) & 1u);
+        if (!__all_sync(0xffffffffu, ok)) {
+            if (lane == 0) raise_error(p.ws, kErrTimeout);
+            break;
+        }
+        const ChunkRef c = chunk_ref(p, (uint32_t)it);
+        const unsigned char* cbuf = ring + (size_t)slot * kChunkBytes;
+        const bool sane = !c.valid || (check_ok(p.ws, c.chunk >= 0 && c.chunk < p.cpr, -111, c.chunk) &&
+                                       check_ok(p.ws, c.slot >= 0 && c.slot < p.slots, -112, c.slot));
+        if (c.valid && sane) {
+            if (!kPrecise || c.slot != 2 * c.ks) {
+                uint4 raw[kLoads];
+#pragma unroll
+                for (int v = 0; v < kLoads; ++v)
+                    raw[v] = *reinterpret_cast<const uint4*>(cbuf + v * 512 + lane * 16);
+                if (c.chunk == p.cpr - 1) {  // the row's last chunk: mask past V
+                    const long long base = (long long)c.chunk * Geo<DT>::kChunk + lane * Geo<DT>::kPerVec;
+#pragma unroll
+                    for (int v = 0; v < kLoads; ++v)
+                        if (base + v * (Geo<DT>::kChunk / kLoads) >= p.R.V)
+                            raw[v] = DT == 0 ? make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u)
+                                             : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+                }
+                const float2 fp = fast_partial<DT>(raw, c.is_draft ? p.sc_d.c2 : p.sc_t.c2, p.ws);
+                if (lane == 0)
+                    ws_ptr<float2>(p.ws, p.L.fast)[((size_t)c.s * p.slots + c.slot) * p.cpr + c.chunk] = fp;
+            } else {
+                constexpr int SUB = Geo<DT>::kSub;
+                const long long e0 = (long long)c.chunk * Geo<DT>::kChunk + (long long)lane * SUB;
+                const SmemBlock<DT> src{cbuf + lane * 128, lane & 7};
+                float4* tot = ws_ptr<float4>(p.ws, p.L.ddtot) + (size_t)(c.s * 2) * p.cpr + c.chunk;
+                float4* sub = ws_ptr<float4>(p.ws, p.L.ddsub) + ((size_t)(c.s * 2) * p.cpr + c.chunk) * kSubs;
+                precise_core<DT>(src, e0 + SUB <= p.R.V, e0, p.R.V, lane, P, tot, sub);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
+        if (c.valid && sane) finish_chunk<DT, MODE>(p, P, c.s, c.ks, lane);
+    }
+}
+
+template <int DT, int MODE>
+static cudaError_t launch_tma_t(const StreamParams& p, cudaStream_t st) {
+    auto kern = stream_tma_kernel<DT, MODE>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const long long cap = device_sm_count();
+    const long long want = (p.items + kTmaConsumers - 1) / kTmaConsumers;
+    int grid = (int)(want < cap ? want : cap);
+    if (grid < 1) grid = 1;
+    kern<<<grid, kTmaThreads, kSmemBytes, st>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_stream_tma(const StreamParams& p, cudaStream_t st) {
+    if (p.dtype == 0) {
+        if (p.mode == kModeSD) return launch_tma_t<0, kModeSD>(p, st);
+        if (p.mode == kModeSMC) return launch_tma_t<0, kModeSMC>(p, st);
+        return launch_tma_t<0, kModeSMCStep>(p, st);
+    }
+    if (p.mode == kModeSD) return launch_tma_t<1, kModeSD>(p, st);
+    if (p.mode == kModeSMC) return launch_tma_t<1, kModeSMC>(p, st);
+    return launch_tma_t<1, kModeSMCStep>(p, st);
+}
+
+}  // namespace smcsd

@@ -18,3 +18,15 @@ extern "C" void probe_dd_recip(const float* ah, const float* al, int n, float* r
         rl[i] = r.lo;
     }
 }
+
+#include "smcsd_fastdiv.h"
+
+// q = n / d through the launch-invariant division, for n in [0, count).
+extern "C" int probe_fast_div_check(unsigned d, unsigned start, unsigned count, unsigned stride) {
+    const smcsd::FastDiv f = smcsd::make_fastdiv(d);
+    for (unsigned i = 0; i < count; ++i) {
+        const unsigned n = start + i * stride;
+        if (smcsd::fast_div(n, f) != n / d) return (int)i + 1;
+    }
+    return 0;
+}

@@ -74,3 +74,14 @@ def test_dd_recip(probe):
     ld = np.longdouble
     err = np.abs((rh.astype(ld) + rl.astype(ld)) * (ah.astype(ld) + al.astype(ld)) - 1)
     assert err.max() < 1e-13
+
+
+@pytest.mark.parametrize("d", [1, 2, 3, 5, 7, 63, 64, 65, 126, 567, 1152, 4097, 72576, 1 << 20, 999983,
+                               (1 << 30) + 3])
+def test_fast_division(probe, d):
+    """The launch-invariant division used to decode chunk indices equals n // d for n < 2^31."""
+    probe.probe_fast_div_check.argtypes = [ctypes.c_uint] * 4
+    probe.probe_fast_div_check.restype = ctypes.c_int
+    assert probe.probe_fast_div_check(d, 0, 200000, 1) == 0
+    assert probe.probe_fast_div_check(d, (1 << 31) - 200001, 200000, 1) == 0
+    assert probe.probe_fast_div_check(d, 12345, 100000, 21473) == 0

@@ -215,3 +215,22 @@ def test_fused_step_equals_separate_calls(smcsd):
                    ("resampled", res_b), ("table_out", tout_b), ("refcount", rc_b)):
         assert torch.equal(a[ka], vb), ka
     assert torch.equal(lw_a, lw_b)
+
+
+def test_workspace_exp_table_cache_across_scales(smcsd):
+    """One workspace, alternating scales alpha/T: the first call publishes its exp table in the
+    workspace, calls with another scale build their own, calls with the first scale reuse it.
+    Every call must match the oracle."""
+    S, K, V = 16, 2, 20000
+    ws = smcsd.Workspace(smcsd.OP_SMC_REWEIGHT, S, K, V)
+    L = DecisionLedger()
+    for i, (T, alpha) in enumerate([(1.0, 1.0), (0.7, 4.0), (1.0, 1.0), (0.7, 4.0), (1.0, 1.0)]):
+        c, u, lw0 = reweight_case(smcsd, 50 + i, S, K, V, T, alpha)
+        lw = dev(lw0.copy())
+        tok = smcsd.smc_reweight(dev_logits(c.tgt), dev_logits(c.drf), dev(c.draft_tokens), S, K, V,
+                                 T, alpha, dev(u), lw, ws=ws)
+        assert smcsd.check_status(ws) == 0
+        o = oracle.smc_reweight(c.tgt, c.drf, c.draft_tokens, S, K, V, T, alpha, u, lw0)
+        L.compare("bonus_token", host(tok), o["bonus_token"], o["bonus_margin"])
+        np.testing.assert_allclose(host(lw), o["logw"], atol=FLOAT_ATOL, rtol=0)
+    L.finish()
