@@ -43,13 +43,20 @@ struct ResidualBlock {
     ResidualCtx c;
     PreciseCtx P;
     static constexpr int PL = Geo<DT>::kSub / kWarp;
-    __device__ __forceinline__ void operator()(int chunk, int sub, int lane, dd (&w)[PL]) const {
+    __device__ __forceinline__ void operator()(int chunk, int sub, int lane, int, dd (&w)[PL]) const {
         const long long e0 = (long long)chunk * Geo<DT>::kChunk + (long long)sub * Geo<DT>::kSub + lane * PL;
 #pragma unroll
         for (int q = 0; q < PL; ++q) {
             const long long e = e0 + q;
             w[q] = e < V ? residual_weight<DT>(logit_bits<DT>(trow, e), logit_bits<DT>(drow, e), c, P)
                          : dd{0.0f, 0.0f};
+        }
+    }
+    __device__ __forceinline__ void prefetch(int chunk, int lane) const {
+        const long long e = (long long)chunk * Geo<DT>::kChunk + (long long)lane * (128 / Geo<DT>::kBytes);
+        if (chunk >= 0 && e < V) {
+            l2_prefetch(static_cast<const char*>(trow) + e * Geo<DT>::kBytes);
+            l2_prefetch(static_cast<const char*>(drow) + e * Geo<DT>::kBytes);
         }
     }
 };

@@ -81,12 +81,15 @@ struct WsLayout {
     size_t cnt_seq3;   // uint32 [S]  third pass (SD)
     size_t cnt_group;  // uint32 [S]
     size_t cnt_misc;   // uint32 [16]
+    size_t claim;      // uint32 [64]  chunk claim counters (one per stripe) and a blocks-done count
     size_t fast;       // float2 [S * (2K+1) * cpr]
     size_t ddtot;      // float4 [S * 2 * cpr]          chunk totals of sampled rows
     size_t ddsub;      // float4 [S * 2 * cpr * kSubs]  lane-block partials of sampled rows
     size_t rtot;       // float4 [S * cpr]              residual chunk totals (SD)
     size_t rsub;       // float4 [S * cpr * kSubs]      residual lane-block partials (SD)
     size_t seq;        // SeqState [S]
+    size_t rowL;       // double [S * (2K+1)]  row normalisers log sum_i exp(c z_i)
+    size_t zsel;       // float  [S * (2K+1)]  logit of the row at its draft token
     size_t tab;        // cached exp table: 4 tag words + 4608 float2 (see setup_exp_table)
     size_t total;
 };
@@ -111,6 +114,8 @@ inline WsLayout ws_layout(int S, int K, int V) {
     o = align256(o + 4 * s);
     L.cnt_misc = o;
     o = align256(o + 4 * 16);
+    L.claim = o;
+    o = align256(o + 4 * 64);
     L.fast = o;
     o = align256(o + 8 * s * (2 * k + 1) * cpr);
     L.ddtot = o;
@@ -123,6 +128,10 @@ inline WsLayout ws_layout(int S, int K, int V) {
     o = align256(o + 16 * s * cpr * kSubs);
     L.seq = o;
     o = align256(o + sizeof(SeqState) * s);
+    L.rowL = o;
+    o = align256(o + 8 * s * (2 * k + 1));
+    L.zsel = o;
+    o = align256(o + 4 * s * (2 * k + 1));
     L.tab = o;
     o = align256(o + 16 + 8 * 4608);
     L.total = o;
@@ -219,13 +228,23 @@ __device__ __forceinline__ double warp_exclusive_scan_d(double v, int lane) {
 // loads
 // ------------------------------------------------------------------------------------------
 
-// Streaming 16-byte load through the non-coherent path, not kept in L1.
-__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+// L2 policy for data read exactly once (the logits): evicted first, so that the stream does not
+// push the small per-row partials, the tables and the epilogues' code out of L2.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+// Streaming 16-byte load through the non-coherent path, not kept in L1, evicted first from L2.
+__device__ __forceinline__ uint4 ld_stream16(const void* p, uint64_t pol) {
     uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
                  : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
+                 : "l"(p), "l"(pol));
     return r;
+}
+__device__ __forceinline__ void l2_prefetch(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 // Coherent L2 loads for data written by other blocks during the same kernel.
 __device__ __forceinline__ float4 ld_cg4(const float4* p) { return __ldcg(p); }
@@ -239,6 +258,22 @@ template <int DT>
 __device__ __forceinline__ uint32_t logit_bits(const void* row, long long i) {
     if (DT == 0) return __ldg(static_cast<const unsigned*>(row) + i);
     return (uint32_t)__ldg(static_cast<const unsigned short*>(row) + i);
+}
+// The same for a streamed element, evicted first from L2.
+template <int DT>
+__device__ __forceinline__ uint32_t logit_bits_stream(const void* row, long long i, uint64_t pol) {
+    if (DT == 0) {
+        uint32_t v;
+        asm volatile("ld.global.nc.L2::cache_hint.u32 %0, [%1], %2;"
+                     : "=r"(v)
+                     : "l"(static_cast<const unsigned*>(row) + i), "l"(pol));
+        return v;
+    }
+    unsigned short v;
+    asm volatile("ld.global.nc.L2::cache_hint.u16 %0, [%1], %2;"
+                 : "=h"(v)
+                 : "l"(static_cast<const unsigned short*>(row) + i), "l"(pol));
+    return (uint32_t)v;
 }
 template <int DT>
 __device__ __forceinline__ float bits_to_float(uint32_t b) {
@@ -289,6 +324,24 @@ __device__ __forceinline__ const void* row_ptr(const void* base, long long row, 
     return static_cast<const char*>(base) + row * (long long)V * Geo<DT>::kBytes;
 }
 
+// Dynamic dealing of the chunks: the items of stripe j are j, j + n, j + 2n, ... (n stripes);
+// claimer j of every block takes the next one from the stripe's counter. Returns -1 when the
+// stripe is used up. The counters start at zero and the last block to finish resets them
+// (reset_claims).
+constexpr int kClaimDone = 63;  // index of the blocks-done count among the claim words
+__device__ __forceinline__ long long claim_item(unsigned* claim, int j, int n, long long items) {
+    const long long it = (long long)atomicAdd(claim + j, 1u) * n + j;
+    return it < items ? it : -1;
+}
+
+// Programmatic dependent launch: the streaming pass lets the finishing pass be scheduled early;
+// the finishing pass waits for the streaming pass to complete (and its writes to be visible)
+// before it reads them. Both are no-ops without a programmatic dependency.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Completion count. Every arrival is a release at device scope (the warp's stores, ordered
 // before lane 0 by the warp barrier, become visible before the count); only the last arriver
 // then takes an acquire fence before it reads what the others stored. The last arriver resets
@@ -317,6 +370,17 @@ __device__ __forceinline__ bool arrive_last(unsigned* counter, unsigned expected
     }
     last = __shfl_sync(0xffffffffu, last, 0);
     return last != 0;
+}
+
+// Called by one thread of each block once all of the block's claimers have stopped: the last
+// block to get here resets the n stripe counters and the blocks-done count for the next call.
+__device__ __forceinline__ void reset_claims(unsigned* claim, int n) {
+    const unsigned old = atom_add_release(claim + kClaimDone, 1u);
+    if (old == gridDim.x - 1) {
+        fence_acquire();
+        for (int j = 0; j < n; ++j) atomicExch(claim + j, 0u);
+        atomicExch(claim + kClaimDone, 0u);
+    }
 }
 
 }  // namespace smcsd

@@ -101,7 +101,8 @@ struct PacerParams {
     WsLayout L;
 };
 
-cudaError_t launch_stream(const StreamParams& p, cudaStream_t st);      // dispatch
+cudaError_t launch_stream(const StreamParams& p, cudaStream_t st);      // both passes
+cudaError_t launch_finish(const StreamParams& p, cudaStream_t st);      // finishing pass
 cudaError_t launch_stream_tma(const StreamParams& p, cudaStream_t st);  // aligned rows
 cudaError_t launch_sd_sample(const SampleParams& p, cudaStream_t st);
 cudaError_t launch_resample(const ResampleParams& p, cudaStream_t st);

@@ -212,14 +212,14 @@ constexpr int kNoMass = INT_MIN / 2;  // n of a chunk without mass
 // chunk*kChunk + v*(kChunk/8) + l*kPerVec + [0, kPerVec). Logits beyond V read as -inf.
 template <int DT>
 __device__ __forceinline__ void load_chunk_interleaved(const void* row, int V, bool vec, int chunk,
-                                                       int lane, uint4 (&raw)[kLoads]) {
+                                                       int lane, uint4 (&raw)[kLoads], uint64_t pol) {
     constexpr int PV = Geo<DT>::kPerVec;
     const long long base = (long long)chunk * Geo<DT>::kChunk + lane * PV;
     if (vec) {
 #pragma unroll
         for (int v = 0; v < kLoads; ++v) {
             const long long e = base + v * (Geo<DT>::kChunk / kLoads);
-            raw[v] = e < V ? ld_stream16(static_cast<const char*>(row) + e * Geo<DT>::kBytes)
+            raw[v] = e < V ? ld_stream16(static_cast<const char*>(row) + e * Geo<DT>::kBytes, pol)
                            : (DT == 0 ? make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u)
                                       : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u));
         }
@@ -231,11 +231,11 @@ __device__ __forceinline__ void load_chunk_interleaved(const void* row, int V, b
             for (int j = 0; j < 4; ++j) {
                 if (DT == 0) {
                     const long long e = base + v * (Geo<DT>::kChunk / kLoads) + j;
-                    w[j] = e < V ? logit_bits<0>(row, e) : 0xff800000u;
+                    w[j] = e < V ? logit_bits_stream<0>(row, e, pol) : 0xff800000u;
                 } else {
                     const long long e = base + v * (Geo<DT>::kChunk / kLoads) + 2 * j;
-                    const uint32_t lo = e < V ? logit_bits<1>(row, e) : 0xff80u;
-                    const uint32_t hi = e + 1 < V ? logit_bits<1>(row, e + 1) : 0xff80u;
+                    const uint32_t lo = e < V ? logit_bits_stream<1>(row, e, pol) : 0xff80u;
+                    const uint32_t hi = e + 1 < V ? logit_bits_stream<1>(row, e + 1, pol) : 0xff80u;
                     w[j] = lo | (hi << 16);
                 }
             }
@@ -472,58 +472,38 @@ __device__ __forceinline__ void precise_partials(const void* row, int V, bool ve
 // row normalisers from fast partials
 // ------------------------------------------------------------------------------------------
 
-// Natural-log normalisers log sum_i exp(c z_i) of up to four rows whose fast partials start at
-// part[r * stride] (cpr chunks each). Returns, on lane r < nrows, the normaliser of row r (NaN
-// for a row without mass); the four rows' partial loads are in flight together.
-__device__ __forceinline__ double rows_lse_fast4(const float2* part, int stride, int nrows, int cpr,
-                                                 const Scale& sc, int lane) {
-    constexpr int RB = 4;
-    float mq[RB], s[RB], M[RB];  // running fl(m c2) of the lane's largest chunk, its sum, max m
-#pragma unroll
-    for (int b = 0; b < RB; ++b) {
-        mq[b] = kNegInf;
-        s[b] = 0.0f;
-        M[b] = kNegInf;
-    }
+// Natural-log normaliser log sum_i exp(c z_i) of one row from its cpr fast partials, on every
+// lane (NaN for a row without mass). The partials' loads are all in flight together.
+__device__ __forceinline__ double row_lse_fast(const float2* part, int cpr, const Scale& sc, int lane) {
+    float mq = kNegInf, s = 0.0f, M = kNegInf;  // running fl(m c2) of the lane's largest chunk, its sum, max m
     for (int c0 = 0; c0 < cpr; c0 += 4 * kWarp) {
-        float2 v[RB][4];
+        float2 v[4];
 #pragma unroll
-        for (int b = 0; b < RB; ++b)
+        for (int j = 0; j < 4; ++j) {
+            const int c = c0 + lane + j * kWarp;
+            v[j] = c < cpr ? ld_cg2(part + c) : make_float2(kNegInf, 0.0f);
+        }
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int c = c0 + lane + j * kWarp;
-                v[b][j] = (b < nrows && c < cpr) ? ld_cg2(part + (size_t)b * stride + c)
-                                                 : make_float2(kNegInf, 0.0f);
+        for (int j = 0; j < 4; ++j) {
+            const float pm = v[j].x, ps = v[j].y;
+            if (pm == kNegInf) continue;
+            M = fmaxf(M, pm);
+            const float q = pm * sc.c2;
+            if (q > mq) {
+                s = s * hw_exp2(mq - q) + ps;
+                mq = q;
+            } else {
+                s += ps * hw_exp2(q - mq);
             }
-#pragma unroll
-        for (int b = 0; b < RB; ++b)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float pm = v[b][j].x, ps = v[b][j].y;
-                if (pm == kNegInf) continue;
-                M[b] = fmaxf(M[b], pm);
-                const float q = pm * sc.c2;
-                if (q > mq[b]) {
-                    s[b] = s[b] * hw_exp2(mq[b] - q) + ps;
-                    mq[b] = q;
-                } else {
-                    s[b] += ps * hw_exp2(q - mq[b]);
-                }
-            }
-    }
-    double out = __longlong_as_double(0x7ff8000000000000ll);
-#pragma unroll
-    for (int b = 0; b < RB; ++b) {
-        const float Mb = warp_max(M[b]);
-        const float Q = Mb * sc.c2;
-        const float t = (mq[b] == kNegInf) ? 0.0f : s[b] * hw_exp2(mq[b] - Q);
-        const float Ssum = warp_sum(t);
-        if (lane == b && Mb != kNegInf && Ssum > 0.0f) {
-            const float rQ = fmaf(Mb, sc.c2, -Q);  // exact residual of fl(M c2)
-            out = sc.c * (double)Mb + log((double)Ssum) - (double)rQ * 0.69314718055994530942;
         }
     }
-    return out;
+    const float Mb = warp_max(M);
+    const float Q = Mb * sc.c2;
+    const float t = (mq == kNegInf) ? 0.0f : s * hw_exp2(mq - Q);
+    const float Ssum = warp_sum(t);
+    if (Mb == kNegInf || !(Ssum > 0.0f)) return __longlong_as_double(0x7ff8000000000000ll);
+    const float rQ = fmaf(Mb, sc.c2, -Q);  // exact residual of fl(M c2)
+    return sc.c * (double)Mb + log((double)Ssum) - (double)rQ * 0.69314718055994530942;
 }
 
 // ------------------------------------------------------------------------------------------
@@ -539,26 +519,45 @@ __device__ __forceinline__ dd part_value(float4 p, int N) {
 
 // Draw token = min{ i : sum_{j<=i} w_j > u * sum_j w_j } over a row whose chunk totals `tot`
 // [cpr] and lane-block partials `sub` [cpr * kSubs] describe the weights, rescanning one lane
-// block with `block_weights(chunk, sub, lane, w[PL])` (PL = kSub / 32 weights per lane, in
+// block with `block_weights(chunk, sub, lane, N, w[PL])` (PL = kSub / 32 weights per lane, in
 // units of 2^N, reproducing the partials exactly). Returns the token on every lane (-1 if the
-// row has no mass). If `lse` is given it receives log(sum_j w_j) + N ln 2.
+// row has no mass). If `lse` is given it receives log(sum_j w_j) + N ln 2. Lane l reads the
+// contiguous chunk totals [l*cpl, l*cpl + cpl) once (kept in registers up to kDrawCache per
+// lane) and serves both the common exponent and the chunk-level walk from them.
+constexpr int kDrawCache = 4;
 template <int PL, typename BlockFn>
 __device__ int draw_inverse_cdf(const float4* tot, const float4* sub, int cpr, int chunk_elems,
                                 int sub_elems, float u, int lane, BlockFn block_weights,
                                 double* lse) {
+    const int cpl = (cpr + kWarp - 1) / kWarp;
+    const int c_begin = min(lane * cpl, cpr), c_end = min(c_begin + cpl, cpr);
+    const bool cached = cpl <= kDrawCache;
+    float4 tc[kDrawCache];
     int N = kNoMass;
-    for (int c = lane; c < cpr; c += kWarp) {
-        const float4 t = ld_cg4(tot + c);
-        if (t.x > 0.0f) N = max(N, __float_as_int(t.z));
+    if (cached) {
+#pragma unroll
+        for (int q = 0; q < kDrawCache; ++q) {
+            tc[q] = c_begin + q < c_end ? ld_cg4(tot + c_begin + q) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (tc[q].x > 0.0f) N = max(N, __float_as_int(tc[q].z));
+        }
+    } else {
+        for (int c = lane; c < cpr; c += kWarp) {
+            const float4 t = ld_cg4(tot + c);
+            if (t.x > 0.0f) N = max(N, __float_as_int(t.z));
+        }
     }
     N = warp_max_i(N);
     if (N == kNoMass) return -1;
 
-    // chunk level: lane l owns the contiguous chunks [l*cpl, l*cpl + cpl)
-    const int cpl = (cpr + kWarp - 1) / kWarp;
-    const int c_begin = min(lane * cpl, cpr), c_end = min(c_begin + cpl, cpr);
+    // chunk level: lane l owns the contiguous chunks [c_begin, c_end)
     dd loc{0.0f, 0.0f};
-    for (int c = c_begin; c < c_end; ++c) loc = dd_add(loc, part_value(ld_cg4(tot + c), N));
+    if (cached) {
+#pragma unroll
+        for (int q = 0; q < kDrawCache; ++q)
+            if (c_begin + q < c_end) loc = dd_add(loc, part_value(tc[q], N));
+    } else {
+        for (int c = c_begin; c < c_end; ++c) loc = dd_add(loc, part_value(ld_cg4(tot + c), N));
+    }
     const dd excl = warp_exclusive_scan_dd(loc, lane);
     const dd incl = dd_add(excl, loc);
     const dd R{__shfl_sync(0xffffffffu, incl.hi, 31), __shfl_sync(0xffffffffu, incl.lo, 31)};
@@ -580,19 +579,26 @@ __device__ int draw_inverse_cdf(const float4* tot, const float4* sub, int cpr, i
         dd p = excl;
         int last_pos = -1;
         dd last_base = p;
-        for (int c = c_begin; c < c_end; ++c) {
-            const dd v = part_value(ld_cg4(tot + c), N);
-            if (v.hi > 0.0f) {
-                last_pos = c;
-                last_base = p;
-                const dd q = dd_add(p, v);
-                if (dd_gt(q, target)) {
-                    c_star = c;
-                    base = p;
-                    break;
-                }
-                p = q;
+        bool found = false;
+        auto visit = [&](int c, dd v) {
+            if (found || !(v.hi > 0.0f)) return;
+            last_pos = c;
+            last_base = p;
+            const dd qq = dd_add(p, v);
+            if (dd_gt(qq, target)) {
+                c_star = c;
+                base = p;
+                found = true;
+            } else {
+                p = qq;
             }
+        };
+        if (cached) {
+#pragma unroll
+            for (int q = 0; q < kDrawCache; ++q)
+                if (c_begin + q < c_end) visit(c_begin + q, part_value(tc[q], N));
+        } else {
+            for (int c = c_begin; c < c_end; ++c) visit(c, part_value(ld_cg4(tot + c), N));
         }
         if (c_star < 0) {
             c_star = last_pos;
@@ -602,6 +608,7 @@ __device__ int draw_inverse_cdf(const float4* tot, const float4* sub, int cpr, i
     c_star = __shfl_sync(0xffffffffu, c_star, owner);
     base.hi = __shfl_sync(0xffffffffu, base.hi, owner);
     base.lo = __shfl_sync(0xffffffffu, base.lo, owner);
+    block_weights.prefetch(c_star, lane);  // the rescan below reads from this chunk
 
     // lane-block level: one block per lane
     const dd sv = part_value(ld_cg4(sub + (size_t)c_star * kSubs + lane), N);
@@ -620,7 +627,7 @@ __device__ int draw_inverse_cdf(const float4* tot, const float4* sub, int cpr, i
 
     // logit level: rescan the block (lane l holds logits l*PL .. l*PL+PL-1 of it)
     dd w[PL];
-    block_weights(c_star, s_star, lane, w);
+    block_weights(c_star, s_star, lane, N, w);
     dd lsum{0.0f, 0.0f};
 #pragma unroll
     for (int q = 0; q < PL; ++q) lsum = dd_add(lsum, w[q]);
@@ -654,10 +661,9 @@ template <int DT>
 struct PreciseBlock {
     const void* row;
     int V;
-    int N;
     PreciseCtx P;
     static constexpr int PL = Geo<DT>::kSub / kWarp;
-    __device__ __forceinline__ void operator()(int chunk, int sub, int lane, dd (&w)[PL]) const {
+    __device__ __forceinline__ void operator()(int chunk, int sub, int lane, int N, dd (&w)[PL]) const {
         const long long e0 = (long long)chunk * Geo<DT>::kChunk + (long long)sub * Geo<DT>::kSub + lane * PL;
 #pragma unroll
         for (int q = 0; q < PL; ++q) {
@@ -666,6 +672,11 @@ struct PreciseBlock {
                        ? precise_weight<DT>(logit_bits<DT>(row, e), N, P)
                        : dd{0.0f, 0.0f};
         }
+    }
+    // pull chunk `chunk` of the row towards L2 (lane l: its 128-byte piece)
+    __device__ __forceinline__ void prefetch(int chunk, int lane) const {
+        const long long e = (long long)chunk * Geo<DT>::kChunk + (long long)lane * (128 / Geo<DT>::kBytes);
+        if (chunk >= 0 && e < V) l2_prefetch(static_cast<const char*>(row) + e * Geo<DT>::kBytes);
     }
 };
 
@@ -690,7 +701,7 @@ template <int DT>
 __device__ __forceinline__ int draw_precise_row(const float4* tot, const float4* sub, int cpr,
                                                 const void* row, int V, const PreciseCtx& P,
                                                 float u, int lane, double* lse) {
-    PreciseBlock<DT> fn{row, V, row_exponent(tot, cpr, lane), P};
+    PreciseBlock<DT> fn{row, V, P};
     return draw_inverse_cdf<PreciseBlock<DT>::PL>(tot, sub, cpr, Geo<DT>::kChunk, Geo<DT>::kSub,
                                                   u, lane, fn, lse);
 }
@@ -711,10 +722,121 @@ __device__ __forceinline__ int children_below(double C, double U, int N) {
     return (int)(j + 1);
 }
 
+// Resampling of a group of at most kWarp * kResamplePer particles with every weight computed
+// once and held in registers (lane l holds particles l*per .. l*per+per-1). The ancestor of
+// child j is the number of particles i with C_i <= v_j = (j + U) / N (C is nondecreasing below
+// 1 and C_{N-1} = 1 > v_j), found by a branch-free binary search over the C_i in the lanes'
+// registers that compares the bit patterns of the nonnegative doubles, which order like the
+// values. The ancestors of the lane's children are also left in anc_reg (N when not resampled).
+constexpr int kResamplePer = 4;
+
+// Value of register q of lane `src`, for a per-lane (src, q); `per` registers are live.
+__device__ __forceinline__ long long shfl_pick(const long long (&v)[kResamplePer], int per, int src, int q) {
+    long long r = 0;
+#pragma unroll
+    for (int q2 = 0; q2 < kResamplePer; ++q2) {
+        if (q2 < per) {
+            const long long t = __shfl_sync(0xffffffffu, v[q2], src);
+            if (q2 == q) r = t;
+        }
+    }
+    return r;
+}
+
+__device__ __forceinline__ bool group_resample_small(float* logw, int N, float thr, float U,
+                                                     int32_t* anc, float* ess_out, int32_t* res_out,
+                                                     void* ws, int lane, int (&anc_reg)[kResamplePer]) {
+    const int per = (N + kWarp - 1) / kWarp;
+    const int i0 = min(lane * per, N), i1 = min(i0 + per, N);
+#pragma unroll
+    for (int q = 0; q < kResamplePer; ++q) anc_reg[q] = i0 + q;
+    float v[kResamplePer];
+    bool bad = false;
+    float m = kNegInf;
+#pragma unroll
+    for (int q = 0; q < kResamplePer; ++q) {
+        v[q] = kNegInf;
+        if (i0 + q < i1) {
+            v[q] = __ldcg(logw + i0 + q);
+            if (v[q] != v[q] || v[q] == kPosInf) bad = true;
+            m = fmaxf(m, v[q]);
+        }
+    }
+    const double M = (double)warp_max(m);
+    bad = __any_sync(0xffffffffu, bad) || M == -__builtin_huge_val();
+    if (bad) {
+        if (lane == 0) raise_error(ws, kErrNonfinite);
+        for (int j = lane; j < N; j += kWarp) anc[j] = j;
+        if (lane == 0 && res_out) *res_out = 0;
+        return false;
+    }
+    double w[kResamplePer];
+    double loc = 0.0, loc2 = 0.0;
+#pragma unroll
+    for (int q = 0; q < kResamplePer; ++q) {
+        w[q] = 0.0;
+        if (q < per) {  // (uniform) every double operation counts: keep them to the live ones
+            if (i0 + q < i1) w[q] = exp((double)v[q] - M);
+            loc += w[q];
+            loc2 += w[q] * w[q];
+        }
+    }
+    const double W = warp_sum_d(loc), W2 = warp_sum_d(loc2);
+    const double ess = W * W / W2;
+    const bool res = ess < (double)thr;
+    if (lane == 0) {
+        if (ess_out) *ess_out = (float)ess;
+        if (res_out) *res_out = res ? 1 : 0;
+    }
+    if (!res) {
+        for (int j = lane; j < N; j += kWarp) anc[j] = j;
+        return false;
+    }
+    long long cb[kResamplePer], vb[kResamplePer];
+    double r = warp_exclusive_scan_d(loc, lane);
+    const double Ud = (double)U;
+#pragma unroll
+    for (int q = 0; q < kResamplePer; ++q) {
+        cb[q] = vb[q] = 0;
+        if (q < per) {
+            r += w[q];
+            const int i = i0 + q;
+            cb[q] = __double_as_longlong(i == N - 1 ? 1.0 : r / W);
+            vb[q] = __double_as_longlong(((double)i + Ud) / (double)N);
+        }
+    }
+    int top = 1;
+    while (top * 2 <= N) top *= 2;
+    int cnt[kResamplePer] = {0, 0, 0, 0};
+    for (int step = top; step > 0; step >>= 1) {
+#pragma unroll
+        for (int q = 0; q < kResamplePer; ++q) {
+            if (q < per) {
+                const int probe = cnt[q] + step - 1;
+                const int pc = min(probe, N - 1);
+                const long long c = shfl_pick(cb, per, pc / per, pc - (pc / per) * per);
+                if (probe < N && c <= vb[q]) cnt[q] += step;
+            }
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < kResamplePer; ++q) {
+        anc_reg[q] = min(cnt[q], N - 1);
+        if (i0 + q < i1) anc[i0 + q] = anc_reg[q];
+    }
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < kResamplePer; ++q)
+        if (i0 + q < i1) logw[i0 + q] = 0.0f;
+    return true;
+}
+
 // logw [N] of one group (float, in/out). Writes ancestors [N], *ess_out, *res_out (if given).
 // Returns whether the group was resampled (on every lane).
-static __device__ __noinline__ bool group_resample(float* logw, int N, float thr, float U, int32_t* anc,
-                                            float* ess_out, int32_t* res_out, void* ws, int lane) {
+// The general path, for groups of any size (used above kWarp * kResamplePer particles).
+static __device__ __noinline__ bool group_resample_general(float* logw, int N, float thr, float U,
+                                                    int32_t* anc, float* ess_out, int32_t* res_out,
+                                                    void* ws, int lane) {
     double M = -__builtin_huge_val();
     bool bad = false;
     for (int i = lane; i < N; i += kWarp) {
@@ -787,6 +909,17 @@ static __device__ __noinline__ bool group_resample(float* logw, int N, float thr
     __syncwarp();
     for (int i = lane; i < N; i += kWarp) logw[i] = 0.0f;
     return true;
+}
+
+// logw [N] of one group (float, in/out). Writes ancestors [N], *ess_out, *res_out (if given).
+// Returns whether the group was resampled (on every lane).
+__device__ __forceinline__ bool group_resample(float* logw, int N, float thr, float U, int32_t* anc,
+                                               float* ess_out, int32_t* res_out, void* ws, int lane) {
+    if (N <= kWarp * kResamplePer) {
+        int anc_reg[kResamplePer];
+        return group_resample_small(logw, N, thr, U, anc, ess_out, res_out, ws, lane, anc_reg);
+    }
+    return group_resample_general(logw, N, thr, U, anc, ess_out, res_out, ws, lane);
 }
 
 }  // namespace smcsd

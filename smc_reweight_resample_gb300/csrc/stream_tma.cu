@@ -1,17 +1,19 @@
 // stream_tma.cu -- the streaming pass over 16-byte-aligned logits rows as a TMA pipeline.
 //
-// One block per SM: a producer warp whose lane 0 moves 4 KB chunks of logits from HBM into a
-// ring of kRing shared-memory slots with the bulk-copy engine (cp.async.bulk, completion counted
-// on one mbarrier per slot), and kTmaConsumers consumer warps that take the block's chunks in
-// order from a shared counter, wait for their slot, compute the chunk's partial (fast or
-// precise, smcsd_sampling.cuh) from shared memory, hand the slot back (a second mbarrier per
-// slot) and count the chunk for its sequence; the last chunk of a sequence runs its epilogue
-// (smcsd_epilogue.cuh). The producer runs up to kRing chunks (96 KB) ahead, so the consumers
-// never wait on HBM latency, and every logit still crosses HBM exactly once.
+// One block per SM: a producer warp that moves 4 KB chunks of logits from HBM into a ring of
+// kRing = 32 shared-memory slots with the bulk-copy engine (cp.async.bulk, completion counted on
+// one mbarrier per slot; lane j of the producer fills slot j), and kTmaConsumers consumer warps
+// that take the slots in the order they were filled from a shared counter, wait for theirs,
+// compute the chunk's partial (fast or precise, smcsd_sampling.cuh) from shared memory, hand
+// the slot back (a second mbarrier per slot) and count the chunk for its row; the last chunk of
+// a row runs the row's epilogue and so on up (smcsd_epilogue.cuh). The producer runs up to
+// kRing chunks (128 KB) ahead, so the consumers never wait on HBM latency, and every logit
+// still crosses HBM exactly once.
 //
-// Chunks are dealt to blocks round-robin (block b owns chunks b, b+B, b+2B, ... of the
-// sequence-major order), so all blocks see the same mix of fast and precise chunks and advance
-// through the sequences together.
+// Chunks (sequence-major order) are dealt dynamically: producer lane j of every block claims the
+// next chunk of stripe j (chunks j, j+32, j+64, ...) from a grid-wide counter. A block that is
+// busy with an epilogue simply claims fewer chunks, and the last chunk of a row, whose warp runs
+// the row's epilogue, lands on whichever block reaches it, so no block collects the epilogues.
 //
 // Every wait is bounded (about 2 s of wall time): a wait that runs out records
 // SMCSD_ERR_TIMEOUT in the workspace and the warp leaves; the producer, before it leaves,
@@ -22,12 +24,15 @@ namespace smcsd {
 
 constexpr int kTmaConsumers = 16;
 constexpr int kTmaThreads = (kTmaConsumers + 1) * kWarp;
-constexpr int kRing = 24;
+constexpr int kRing = kWarp;  // one slot per producer lane
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 constexpr size_t kSmemRing = (size_t)kRing * kChunkBytes;
 constexpr size_t kSmemTab = (size_t)kTabSize * sizeof(float2);
-constexpr size_t kSmemBytes = kSmemRing + kSmemTab + sizeof(Exp2Table) + 2 * kRing * 8 + kRing * 4 + 16;
+constexpr size_t kSmemBytes =
+    kSmemRing + kSmemTab + sizeof(Exp2Table) + 2 * kRing * 8 + kRing * 8 + kRing * 4 + 16;
+constexpr uint32_t kTagNone = 0xffffffffu;  // slot never loaded
+constexpr uint32_t kTagDone = 0xfffffffeu;  // the slot's claimer has no more chunks
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -78,21 +83,26 @@ __device__ __forceinline__ uint32_t tag_load(uint32_t addr) {
     asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
     return v;
 }
-// Wait (at most kWaitLimitNs) until the tag at `addr` reads k.
-__device__ __forceinline__ bool tag_wait(uint32_t addr, uint32_t k) {
-    if (tag_load(addr) == k) return true;
+// Wait (at most kWaitLimitNs) until the tag at `addr` reads k or kTagDone; the tag seen is
+// left in `seen`.
+__device__ __forceinline__ bool tag_wait(uint32_t addr, uint32_t k, uint32_t& seen) {
+    seen = tag_load(addr);
+    if (seen == k || seen == kTagDone) return true;
     const unsigned long long t0 = global_ns();
-    while (tag_load(addr) != k)
+    for (;;) {
+        seen = tag_load(addr);
+        if (seen == k || seen == kTagDone) return true;
         if (global_ns() - t0 > kWaitLimitNs) return false;
-    return true;
+    }
 }
 
-// 1-D bulk copy global -> shared, completion counted in bytes on `bar`.
+// 1-D bulk copy global -> shared, completion counted in bytes on `bar`, with L2 policy `pol`.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
+                                          uint32_t bar, uint64_t pol) {
     asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-        "l"(src), "r"(bytes), "r"(bar)
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(pol)
         : "memory");
 }
 
@@ -112,49 +122,72 @@ struct SmemBlock {
     }
 };
 
-// The producer (one thread) issues the block's chunks in order, each into slot k % kRing once
-// the consumer of that slot's previous chunk has handed it back, tagging the slot with k first.
+// The producer warp: lane j owns slot j. It claims chunks from stripe j of the grid-wide
+// dealing (claim_item) and loads each into its slot once the consumer of the slot's previous
+// chunk has handed the slot back, recording the chunk's index and then tagging the slot with
+// the block-local sequence number k = 32 * round + j. A lane whose stripe is used up tags its
+// slot kTagDone. The lanes poll their slots together (one non-blocking test per lane per pass),
+// so no lane spins alone while the others wait on it. The next claim is made as soon as a chunk
+// is issued, so its latency overlaps the wait for the slot.
 template <int DT>
 __device__ __noinline__ void tma_producer(const StreamParams& p, unsigned char* ring,
-                                          uint64_t* full, uint64_t* empty, uint32_t* tag) {
-    const uint32_t B = gridDim.x;
+                                          uint64_t* full, uint64_t* empty, uint32_t* tag,
+                                          long long* slot_item, unsigned* n_done, int lane) {
+    unsigned* claim = ws_ptr<unsigned>(p.ws, p.L.claim);
     const long long row_bytes = (long long)p.R.V * Geo<DT>::kBytes;
-    uint32_t k = 0;
-    for (;; ++k) {
-        const long long it = (long long)blockIdx.x + (long long)k * B;
-        if (it >= p.items) break;
-        const int slot = (int)(k % kRing);
-        const uint32_t round = k / kRing;
-        if (round > 0 && !mbar_wait(smem_u32(&empty[slot]), (round - 1) & 1u)) {
-            raise_error(p.ws, kErrTimeout);
-            break;
+    const uint32_t fb = smem_u32(&full[lane]), eb = smem_u32(&empty[lane]);
+    const uint32_t tb = smem_u32(&tag[lane]);
+    const uint32_t dst = smem_u32(ring + (size_t)lane * kChunkBytes);
+    const uint64_t pol = l2_evict_first();
+    long long it = claim_item(claim, lane, kRing, p.items);
+    uint32_t round = 0;
+    bool done = false;
+    unsigned long long t_last = global_ns();
+    while (__any_sync(0xffffffffu, !done)) {
+        if (done) continue;
+        if (round > 0 && !mbar_try_wait(eb, (round - 1) & 1u)) {
+            if (global_ns() - t_last > kWaitLimitNs) {
+                raise_error(p.ws, kErrTimeout);
+                it = -1;  // give the slot up below so that its consumers stop
+            } else {
+                continue;
+            }
+        }
+        if (it < 0) {
+            atomicAdd(n_done, 1u);
+            tag_store(tb, kTagDone);
+            done = true;
+            continue;
         }
         const ChunkRef c = chunk_ref(p, (uint32_t)it);
-        const uint32_t fb = smem_u32(&full[slot]);
-        tag_store(smem_u32(&tag[slot]), k);
         const long long off = (long long)c.chunk * kChunkBytes;
         const long long left = row_bytes - off;
         const uint32_t bytes = (uint32_t)(left < kChunkBytes ? left : kChunkBytes);
         const char* src = static_cast<const char*>(c.is_draft ? p.R.drf : p.R.tgt) +
                           c.row * row_bytes + off;
-        const uint32_t dst = smem_u32(ring + (size_t)slot * kChunkBytes);
         const long long nrows = (long long)p.R.S * (c.is_draft ? p.R.K : p.R.K + 1);
         const bool sane = !c.valid ||
                           (check_ok(p.ws, c.s >= 0 && c.s < p.R.S, -101, it) &&
                            check_ok(p.ws, p.R.toff || (c.row >= 0 && c.row < nrows), -102, c.row) &&
                            check_ok(p.ws, left > 0 && (bytes & 15u) == 0, -103, left) &&
-                           check_ok(p.ws, ((uintptr_t)src & 15u) == 0 && (dst & 15u) == 0, -104,
+                           check_ok(p.ws, ((uintptr_t)src & 15u) == 0, -104,
                                     (long long)(uintptr_t)src));
+        slot_item[lane] = it;
+        tag_store(tb, round * kRing + (uint32_t)lane);
         if (c.valid && sane) {
             mbar_arrive_expect_tx(fb, bytes);
-            bulk_load(dst, src, bytes, fb);
+            bulk_load(dst, src, bytes, fb, pol);
         } else {
             mbar_arrive(fb);
         }
+        ++round;
+        it = claim_item(claim, lane, kRing, p.items);
+        t_last = global_ns();
     }
-    // the copies of the last kRing chunks may still be in flight: wait for them before leaving
-    const uint32_t first = k > (uint32_t)kRing ? k - kRing : 0u;
-    for (uint32_t j = first; j < k; ++j) mbar_wait(smem_u32(&full[j % kRing]), (j / kRing) & 1u);
+    __syncwarp();
+    if (lane == 0) reset_claims(claim, kRing);
+    // the copy of this lane's last chunk may still be in flight: wait for it before leaving
+    if (round > 0) mbar_wait(fb, (round - 1) & 1u);
 }
 
 template <int DT, int MODE>
@@ -167,22 +200,26 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     Exp2Table* sT = reinterpret_cast<Exp2Table*>(smem + kSmemRing + kSmemTab);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSmemRing + kSmemTab + sizeof(Exp2Table));
     uint64_t* empty = full + kRing;
-    uint32_t* tag = reinterpret_cast<uint32_t*>(empty + kRing);
+    long long* slot_item = reinterpret_cast<long long*>(empty + kRing);
+    uint32_t* tag = reinterpret_cast<uint32_t*>(slot_item + kRing);
     unsigned* next = tag + kRing;
+    unsigned* n_done = next + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int i = 0; i < kRing; ++i) {
             mbar_init(smem_u32(&full[i]), 1);
             mbar_init(smem_u32(&empty[i]), 1);
-            tag[i] = 0xffffffffu;
+            tag[i] = kTagNone;
         }
         *next = 0;
+        *n_done = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    if (threadIdx.x == 0) griddep_launch_dependents();
     if (warp == 0) {
-        if (lane == 0) tma_producer<DT>(p, ring, full, empty, tag);
+        tma_producer<DT>(p, ring, full, empty, tag, slot_item, n_done, lane);
         return;
     }
 
@@ -199,20 +236,30 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                         ws_ptr<float2>(p.ws, p.L.tab + 16), p.direct, tid, nthr, 1);
         P.tab = sTab;
     }
-    const long long B = gridDim.x;
     for (;;) {
         unsigned k = 0;
         if (lane == 0) k = atomicAdd(next, 1u);
         k = __shfl_sync(0xffffffffu, k, 0);
-        const long long it = (long long)blockIdx.x + (long long)k * B;
-        if (it >= p.items) break;
         const int slot = (int)(k % kRing);
-        const bool ok = tag_wait(smem_u32(&tag[slot]), k) && mbar_wait(smem_u32(&full[slot]), (k / kRing) & 1u);
-        if (!__all_sync(0xffffffffu, ok)) {
+        uint32_t seen;
+        if (!__all_sync(0xffffffffu, tag_wait(smem_u32(&tag[slot]), k, seen))) {
             if (lane == 0) raise_error(p.ws, kErrTimeout);
             break;
         }
+        if (__shfl_sync(0xffffffffu, seen, 0) == kTagDone) {
+            // this slot has no more chunks; stop once no slot has any
+            unsigned nd = 0;
+            if (lane == 0) nd = *reinterpret_cast<volatile unsigned*>(n_done);
+            if (__shfl_sync(0xffffffffu, nd, 0) == (unsigned)kRing) break;
+            continue;
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full[slot]), (k / kRing) & 1u))) {
+            if (lane == 0) raise_error(p.ws, kErrTimeout);
+            break;
+        }
+        const long long it = *reinterpret_cast<volatile long long*>(&slot_item[slot]);
         const ChunkRef c = chunk_ref(p, (uint32_t)it);
+        const int x = (lane == 0 && c.valid) ? chunk_token(p, c.s, c.slot, c.ks) : -1;
         const unsigned char* cbuf = ring + (size_t)slot * kChunkBytes;
         const bool sane = !c.valid || (check_ok(p.ws, c.chunk >= 0 && c.chunk < p.cpr, -111, c.chunk) &&
                                        check_ok(p.ws, c.slot >= 0 && c.slot < p.slots, -112, c.slot));
@@ -242,9 +289,13 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                 precise_core<DT>(src, e0 + SUB <= p.R.V, e0, p.R.V, lane, P, tot, sub);
             }
         }
+        if (lane == 0 && c.valid && sane && x >= 0)
+            capture_token_logit<DT>(p, c.s, c.slot, c.chunk, x, [&](int off) {
+                return bits_to_float<DT>(DT == 1 ? (uint32_t)reinterpret_cast<const unsigned short*>(cbuf)[off]
+                                                 : reinterpret_cast<const uint32_t*>(cbuf)[off]);
+            });
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
-        if (c.valid && sane) finish_chunk<DT, MODE>(p, P, c.s, c.ks, lane);
     }
 }
 

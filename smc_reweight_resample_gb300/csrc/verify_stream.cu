@@ -2,8 +2,8 @@
 // global loads, used when the rows are not 16-byte aligned (the aligned case runs the TMA
 // pipeline in stream_tma.cu). Same chunk partials and epilogues (smcsd_epilogue.cuh).
 //
-// One 640-thread block per SM, 20 warps taking chunks as they become free; every logit is read
-// from HBM exactly once. Rows that are drawn from (the (K+1)-th target row of each particle) take
+// One 640-thread block per SM, 20 warps claiming chunks from the grid-wide dealing as they become
+// free; every logit is read from HBM exactly once. Rows that are drawn from (the (K+1)-th target row of each particle) take
 // the precise path with the block's shared-memory exp table.
 #include "smcsd_epilogue.cuh"
 
@@ -24,20 +24,22 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                         ws_ptr<float2>(p.ws, p.L.tab + 16), p.direct, threadIdx.x, blockDim.x, 0);
         P.tab = sTab;
     }
-    // Items (chunks, sequence-major) are dealt to blocks round-robin: block b owns items
-    // b, b + B, b + 2B, ... so that every block sees the same mix of fast and precise chunks and
-    // all blocks advance through the sequences together. Within a block, warps take the block's
-    // next item from a shared-memory counter as they become free.
-    __shared__ unsigned next_item;
-    if (threadIdx.x == 0) next_item = 0;
-    __syncthreads();
-    const int lane = threadIdx.x & 31;
+    // Items (chunks, sequence-major) are dealt dynamically: warp w of every block claims the next
+    // chunk of stripe w (chunks w, w + W, w + 2W, ... for W warps per block) from a grid-wide
+    // counter, and claims its following chunk before it works on the current one.
+    if (threadIdx.x == 0) griddep_launch_dependents();
+    constexpr int W = kStreamThreads / kWarp;
+    unsigned* claim = ws_ptr<unsigned>(p.ws, p.L.claim);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint64_t pol = l2_evict_first();
+    long long nxt = 0;
+    if (lane == 0) nxt = claim_item(claim, warp, W, p.items);
+    nxt = __shfl_sync(0xffffffffu, nxt, 0);
     for (;;) {
-        unsigned kk = 0;
-        if (lane == 0) kk = atomicAdd(&next_item, 1u);
-        kk = __shfl_sync(0xffffffffu, kk, 0);
-        const long long it = (long long)blockIdx.x + (long long)kk * gridDim.x;
-        if (it >= p.items) break;
+        const long long it = nxt;
+        if (it < 0) break;
+        if (lane == 0) nxt = claim_item(claim, warp, W, p.items);
+        nxt = __shfl_sync(0xffffffffu, nxt, 0);
         const ChunkRef c = chunk_ref(p, (uint32_t)it);
         if (!c.valid) continue;
         const int s = c.s, slot = c.slot, chunk = c.chunk, ks = c.ks;
@@ -45,7 +47,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         const void* rp = row_ptr<DT>(is_draft ? p.R.drf : p.R.tgt, c.row, p.R.V);
         if (!kPrecise || slot != 2 * ks) {
             uint4 raw[kLoads];
-            load_chunk_interleaved<DT>(rp, p.R.V, p.vec, chunk, lane, raw);
+            load_chunk_interleaved<DT>(rp, p.R.V, p.vec, chunk, lane, raw, pol);
             const float2 fp = fast_partial<DT>(raw, is_draft ? p.sc_d.c2 : p.sc_t.c2, p.ws);
             if (lane == 0)
                 ws_ptr<float2>(p.ws, p.L.fast)[((size_t)s * p.slots + slot) * p.cpr + chunk] = fp;
@@ -54,8 +56,15 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             float4* sub = ws_ptr<float4>(p.ws, p.L.ddsub) + ((size_t)(s * 2) * p.cpr + chunk) * kSubs;
             precise_partials<DT>(rp, p.R.V, p.vec, chunk, lane, P, tot, sub);
         }
-        finish_chunk<DT, MODE>(p, P, s, ks, lane);
+        if (lane == 0 && slot < 2 * ks) {
+            const int x = chunk_token(p, s, slot, ks);
+            capture_token_logit<DT>(p, s, slot, chunk, x, [&](int off) {
+                return logit_at<DT>(rp, (long long)chunk * Geo<DT>::kChunk + off);
+            });
+        }
     }
+    __syncthreads();
+    if (threadIdx.x == 0) reset_claims(claim, W);
 }
 
 int device_sm_count() {
@@ -77,7 +86,7 @@ static cudaError_t launch_stream_t(const StreamParams& p, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_stream(const StreamParams& p, cudaStream_t st) {
+static cudaError_t launch_stream_pass(const StreamParams& p, cudaStream_t st) {
     if (p.vec) return launch_stream_tma(p, st);
     if (p.dtype == 0) {
         if (p.mode == kModeSD) return launch_stream_t<0, kModeSD>(p, st);
@@ -87,6 +96,11 @@ cudaError_t launch_stream(const StreamParams& p, cudaStream_t st) {
     if (p.mode == kModeSD) return launch_stream_t<1, kModeSD>(p, st);
     if (p.mode == kModeSMC) return launch_stream_t<1, kModeSMC>(p, st);
     return launch_stream_t<1, kModeSMCStep>(p, st);
+}
+
+cudaError_t launch_stream(const StreamParams& p, cudaStream_t st) {
+    const cudaError_t e = launch_stream_pass(p, st);
+    return e != cudaSuccess ? e : launch_finish(p, st);
 }
 
 }  // namespace smcsd
