@@ -191,6 +191,34 @@ int smc_step(const void* tgt_logits, const void* drf_logits, int dtype,
              int pages_per_seq, int32_t* refcount, int num_pages,
              void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * smc_step without a workspace argument. None of the pages has a counterpart: this is an
+ * interface variant of smc_step (same step, same arguments and results, minus ws / ws_bytes)
+ * for callers that cannot allocate device memory for a workspace, such as a host program with no
+ * device allocator or a plugin that must not use its host's allocator. The call allocates
+ * nothing: its scratch is a 32 MiB device area owned by this library (SMCSD_STATIC_SCRATCH_BYTES),
+ * set aside when the library's device code is loaded.
+ *   status: optional int32 device pointer; receives this call's device-side status (SMCSD_OK or
+ *     a negative SMCSD_* code, as smcsd_check_status would report), written in stream order.
+ *     Without it, device-side errors of the call are not reported.
+ * Returns SMCSD_ERR_WORKSPACE, before any device work, when the shape needs more scratch than the
+ * area holds (smcsd_workspace_size(SMCSD_OP_SMC_STEP, G*N, K, V) > SMCSD_STATIC_SCRATCH_BYTES),
+ * and the host-side errors of smc_step otherwise.
+ * Each call clears, on the stream, the part of the scratch that must start at zero. All calls on
+ * one device share the one area: calls whose device work may overlap (different streams, or
+ * several host threads without ordering between them) race on it and give wrong results, so
+ * order them, for instance on one stream. The first call on a device looks the area's address up
+ * with that device current; make that first call before any stream capture begins.
+ */
+#define SMCSD_STATIC_SCRATCH_BYTES (32u << 20)
+int smc_step_static(const void* tgt_logits, const void* drf_logits, int dtype,
+                    const int32_t* draft_tokens, int G, int N, int K, int V, float temperature,
+                    float alpha, const float* bonus_uniforms, float* logw, int32_t* bonus_token,
+                    float ess_threshold, const float* resample_uniforms, int32_t* ancestors,
+                    float* ess, int32_t* resampled, const int32_t* table_in, int32_t* table_out,
+                    int pages_per_seq, int32_t* refcount, int num_pages, int32_t* status,
+                    void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -51,8 +51,11 @@ def load(path: str = LIB_PATH):
     lib.pacer_block_stop.argtypes = [P, P, f, i, i, i, i, f, f, P, P, P, P, P, sz, P]
     lib.smc_step.argtypes = [P, P, i, P, i, i, i, i, f, f, P, P, P, f, P, P, P, P, P, P, i, P, i,
                              P, sz, P]
+    lib.smc_step_static.argtypes = [P, P, i, P, i, i, i, i, f, f, P, P, P, f, P, P, P, P, P, P, i,
+                                    P, i, P, P]
     for fn in ("smcsd_workspace_init", "smcsd_check_status", "sd_verify", "smc_reweight",
-               "smc_ess_resample", "kv_pagetable_remap", "pacer_block_stop", "smc_step"):
+               "smc_ess_resample", "kv_pagetable_remap", "pacer_block_stop", "smc_step",
+               "smc_step_static"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -227,5 +230,40 @@ def smc_step(tgt_logits, drf_logits, draft_tokens, G, N, K, V, temperature, alph
                          _ptr(table_in), _ptr(table_out), pages_per_seq, _ptr(refcount), num_pages,
                          w, n, _stream(stream))
     _check(rc, "smc_step")
+    return dict(bonus_token=bonus_token, ancestors=ancestors, ess=ess, resampled=resampled,
+                table_out=table_out, refcount=refcount)
+
+
+STATIC_SCRATCH_BYTES = 32 << 20
+
+
+def smc_step_static(tgt_logits, drf_logits, draft_tokens, G, N, K, V, temperature, alpha,
+                    bonus_uniforms, logw, ess_threshold, resample_uniforms, table_in=None,
+                    pages_per_seq=0, num_pages=0, bonus_token=None, ancestors=None, ess=None,
+                    resampled=None, table_out=None, refcount=None, with_refcount=True,
+                    status=None, stream=None):
+    """smc_step on the library's own scratch area (no workspace argument). Output tensors must
+    be passed in by a caller that cannot allocate; missing ones are allocated here for
+    convenience. `status` (int32 [1] on the device) receives the call's device-side status."""
+    dev = tgt_logits.device
+    S = G * N
+    bonus_token = _out(bonus_token, (S,), torch.int32, dev)
+    ancestors = _out(ancestors, (S,), torch.int32, dev)
+    ess = _out(ess, (G,), torch.float32, dev)
+    resampled = _out(resampled, (G,), torch.int32, dev)
+    if table_in is not None:
+        table_out = _out(table_out, table_in.shape, torch.int32, dev)
+        if with_refcount and refcount is None:
+            refcount = torch.empty(num_pages, dtype=torch.int32, device=dev)
+    else:
+        table_out = refcount = None
+    rc = load().smc_step_static(_ptr(tgt_logits), _ptr(drf_logits), _dtype_code(tgt_logits),
+                                _ptr(draft_tokens), G, N, K, V, float(temperature), float(alpha),
+                                _ptr(bonus_uniforms), _ptr(logw), _ptr(bonus_token),
+                                float(ess_threshold), _ptr(resample_uniforms), _ptr(ancestors),
+                                _ptr(ess), _ptr(resampled), _ptr(table_in), _ptr(table_out),
+                                pages_per_seq, _ptr(refcount), num_pages, _ptr(status),
+                                _stream(stream))
+    _check(rc, "smc_step_static")
     return dict(bonus_token=bonus_token, ancestors=ancestors, ess=ess, resampled=resampled,
                 table_out=table_out, refcount=refcount)

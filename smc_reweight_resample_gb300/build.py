@@ -18,7 +18,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsmcsd.so")
-SOURCES = ["api.cu", "verify_stream.cu", "stream_tma.cu", "finish.cu", "sd_sample.cu", "resample_pacer.cu"]
+SOURCES = ["api.cu", "verify_stream.cu", "stream_tma.cu", "finish.cu", "sd_sample.cu", "resample_pacer.cu",
+           "static_scratch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
