@@ -117,6 +117,7 @@ extern "C" int sd_verify(const void* tgt_logits, const void* drf_logits, int dty
     p.L = L;
     p.cpr = chunks_per_row(V, dtype);
     p.slots = 2 * K + 1;
+    if (p.slots >= (1 << 15)) p.vec = false;  // the pipelined pass packs row slot and draft count in 16 bits each
     p.items = (long long)S * p.slots * p.cpr;
     if (p.items >= (1ll << 31)) return SMCSD_ERR_INVALID_ARG;
     p.div_seq = make_fastdiv((uint32_t)(p.slots * p.cpr));
@@ -168,6 +169,7 @@ static int smc_common(const void* tgt_logits, const void* drf_logits, int dtype,
     p.L = L;
     p.cpr = chunks_per_row(V, dtype);
     p.slots = 2 * K + 1;
+    if (p.slots >= (1 << 15)) p.vec = false;  // the pipelined pass packs row slot and draft count in 16 bits each
     p.items = (long long)S * p.slots * p.cpr;
     if (p.items >= (1ll << 31)) return SMCSD_ERR_INVALID_ARG;
     p.div_seq = make_fastdiv((uint32_t)(p.slots * p.cpr));

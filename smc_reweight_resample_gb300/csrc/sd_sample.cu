@@ -114,7 +114,7 @@ __device__ __noinline__ void sd_rows_epilogue(const SampleParams& p, const Preci
 template <int DT>
 __global__ void __launch_bounds__(kSampleThreads) sd_rows_kernel(const __grid_constant__ SampleParams p) {
     __shared__ Exp2Table sT;
-    __shared__ float2 sTab[DT == 1 ? kTabSize : 1];
+    __shared__ float2 sTab[DT == 1 ? kTabAlloc : 1];
     load_exp2_table_s(p.T, sT);
     PreciseCtx P{p.sc, &sT, nullptr, p.ws, p.direct};
     if (DT == 1 && p.use_table) {
@@ -175,7 +175,7 @@ template <int DT>
 __global__ void __launch_bounds__(kSampleThreads)
     sd_residual_kernel(const __grid_constant__ SampleParams p) {
     __shared__ Exp2Table sT;
-    __shared__ float2 sTab[DT == 1 ? kTabSize : 1];
+    __shared__ float2 sTab[DT == 1 ? kTabAlloc : 1];
     load_exp2_table_s(p.T, sT);
     PreciseCtx P{p.sc, &sT, nullptr, p.ws, p.direct};
     if (DT == 1 && p.use_table) {

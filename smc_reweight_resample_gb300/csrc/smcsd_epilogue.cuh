@@ -26,23 +26,7 @@ __device__ __forceinline__ void load_exp2_table(const Exp2Table& src, Exp2Table&
     __syncthreads();
 }
 
-// The draft token of a chunk's row (target or draft row k < ks of its sequence), or -1 for the
-// bonus row.
-__device__ __forceinline__ int chunk_token(const StreamParams& p, int s, int slot, int ks) {
-    return slot < 2 * ks ? __ldg(p.R.toks + drow_of(p.R, s, slot >> 1)) : -1;
-}
-
-// If the chunk holds its row's draft token x, record the logit there (read by `at`, given the
-// offset within the chunk) for the sequence epilogue.
-template <int DT, typename At>
-__device__ __forceinline__ void capture_token_logit(const StreamParams& p, int s, int slot, int chunk,
-                                                    int x, At at) {
-    const long long off = (long long)x - (long long)chunk * Geo<DT>::kChunk;
-    if (x >= 0 && x < p.R.V && off >= 0 && off < Geo<DT>::kChunk)
-        ws_ptr<float>(p.ws, p.L.zsel)[(size_t)s * p.slots + slot] = at((int)off);
-}
-
-// End of one row (its last chunk's warp): the row's normaliser, or, for the bonus row of a
+// One row: the row's normaliser and the logit at its draft token, or, for the bonus row of a
 // particle, the (K+1)-th token drawn from pi with the row's normaliser as a by-product.
 template <int DT, int MODE>
 __device__ __noinline__ void row_epilogue(const StreamParams& p, const PreciseCtx& P, int s, int slot,
@@ -65,9 +49,18 @@ __device__ __noinline__ void row_epilogue(const StreamParams& p, const PreciseCt
     }
     const bool is_draft = slot < 2 * ks && (slot & 1);
     const size_t r = (size_t)s * p.slots + slot;
+    // the logit at the row's draft token (its load overlaps the normaliser's)
+    float zx = 0.0f;
+    if (lane == 0 && slot < 2 * ks) {
+        const int x = __ldg(R.toks + drow_of(R, s, k));
+        if (x >= 0 && x < R.V)
+            zx = is_draft ? logit_at<DT>(row_ptr<DT>(R.drf, drow_of(R, s, k), R.V), x)
+                          : logit_at<DT>(row_ptr<DT>(R.tgt, trow_of(R, s, k), R.V), x);
+    }
     const double L = row_lse_fast(ws_ptr<float2>(p.ws, p.L.fast) + r * p.cpr, p.cpr,
                                   is_draft ? p.sc_d : p.sc_t, lane);
     if (lane == 0) {
+        if (slot < 2 * ks) ws_ptr<float>(p.ws, p.L.zsel)[r] = zx;
         if (!(L == L)) raise_error(p.ws, kErrNonfinite);  // a row without mass
         ws_ptr<double>(p.ws, p.L.rowL)[r] = L;
         if (is_draft) {

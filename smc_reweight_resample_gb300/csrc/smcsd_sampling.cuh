@@ -41,6 +41,7 @@ constexpr uint32_t kTabMagLo = 0x3980u;        // bf16 bits of 2^-12
 constexpr uint32_t kTabMagHi = 0x4280u;        // bf16 bits of 64
 constexpr uint32_t kTabHalf = kTabMagHi - kTabMagLo;  // entries per sign
 constexpr int kTabSize = 2 * (int)kTabHalf;    // 4608
+constexpr int kTabAlloc = kTabSize + 2;         // entries a table takes: kTabSize and kTabSize+1 are zero
 // the table is used only while |64 * c2| stays far inside floor_int's range
 constexpr double kTabMaxScale = 4096.0;
 
@@ -120,6 +121,8 @@ __device__ __forceinline__ void setup_exp_table(float2* tab, const Scale& sc, co
                                                 int tid, int nthr, int bar) {
     __shared__ int state;  // 0: build and publish, 1: copy, 2: build only
     if (tid == 0) {
+        tab[kTabSize] = make_float2(0.0f, 0.0f);  // the zero entries (never published or copied)
+        tab[kTabSize + 1] = make_float2(0.0f, 0.0f);
         uint32_t magic;
         asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(magic) : "l"(gtag) : "memory");
         if (magic != kTabMagic)
@@ -279,27 +282,61 @@ __device__ __forceinline__ void load_lane_block(const void* row, int V, bool vec
 // chunk partials
 // ------------------------------------------------------------------------------------------
 
+// Packed pairs of floats for the f32x2 instructions of sm_100 and later.
+__device__ __forceinline__ unsigned long long f2_pack(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float2 f2_unpack(unsigned long long v) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return make_float2(lo, hi);
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // Fast partial of one chunk: {m, sum_i 2^(z_i c2 - fl(m c2))} with m the chunk's largest logit
-// (raw, before scaling; c > 0 keeps the order). An all-masked chunk gives {-inf, 0}.
+// (raw, before scaling; c > 0 keeps the order). An all-masked chunk gives {-inf, 0}. The maximum
+// runs as four independent chains; the exponent arguments and the sums as float pairs.
 template <int DT>
 __device__ __forceinline__ float2 fast_partial(const uint4 (&raw)[kLoads], float c2, void* ws) {
     float m;
     if (DT == 1) {
-        __nv_bfloat162 mx = *reinterpret_cast<const __nv_bfloat162*>(&raw[0].x);
+        __nv_bfloat162 mx[4];
 #pragma unroll
-        for (int v = 0; v < kLoads; ++v) {
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t w = j == 0 ? raw[0].x : j == 1 ? raw[0].y : j == 2 ? raw[0].z : raw[0].w;
+            mx[j] = *reinterpret_cast<const __nv_bfloat162*>(&w);
+        }
+#pragma unroll
+        for (int v = 1; v < kLoads; ++v) {
             const uint32_t w[4] = {raw[v].x, raw[v].y, raw[v].z, raw[v].w};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&w[j]));
+            for (int j = 0; j < 4; ++j) mx[j] = __hmax2(mx[j], *reinterpret_cast<const __nv_bfloat162*>(&w[j]));
         }
-        const uint32_t mw = *reinterpret_cast<const uint32_t*>(&mx);
+        const __nv_bfloat162 mm = __hmax2(__hmax2(mx[0], mx[1]), __hmax2(mx[2], mx[3]));
+        const uint32_t mw = *reinterpret_cast<const uint32_t*>(&mm);
         m = fmaxf(bf16_lo(mw), bf16_hi(mw));
     } else {
-        m = kNegInf;
+        float mf[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
 #pragma unroll
-        for (int v = 0; v < kLoads; ++v)
-            m = fmaxf(fmaxf(m, fmaxf(__uint_as_float(raw[v].x), __uint_as_float(raw[v].y))),
-                      fmaxf(__uint_as_float(raw[v].z), __uint_as_float(raw[v].w)));
+        for (int v = 0; v < kLoads; ++v) {
+            mf[0] = fmaxf(mf[0], __uint_as_float(raw[v].x));
+            mf[1] = fmaxf(mf[1], __uint_as_float(raw[v].y));
+            mf[2] = fmaxf(mf[2], __uint_as_float(raw[v].z));
+            mf[3] = fmaxf(mf[3], __uint_as_float(raw[v].w));
+        }
+        m = fmaxf(fmaxf(mf[0], mf[1]), fmaxf(mf[2], mf[3]));
     }
     m = warp_max(m);
     if (m == kNegInf) {
@@ -319,23 +356,27 @@ __device__ __forceinline__ float2 fast_partial(const uint4 (&raw)[kLoads], float
         return make_float2(kNegInf, 0.0f);
     }
     const float nmc2 = -(m * c2);
-    float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+    const unsigned long long C2 = f2_pack(c2, c2), NM = f2_pack(nmc2, nmc2);
+    unsigned long long acc[4] = {0ull, 0ull, 0ull, 0ull};  // (+0.0f, +0.0f) pairs
 #pragma unroll
     for (int v = 0; v < kLoads; ++v) {
         const uint32_t w[4] = {raw[v].x, raw[v].y, raw[v].z, raw[v].w};
         if (DT == 1) {
-            a0 += hw_exp2(fmaf(bf16_lo(w[0]), c2, nmc2)) + hw_exp2(fmaf(bf16_hi(w[0]), c2, nmc2));
-            a1 += hw_exp2(fmaf(bf16_lo(w[1]), c2, nmc2)) + hw_exp2(fmaf(bf16_hi(w[1]), c2, nmc2));
-            a2 += hw_exp2(fmaf(bf16_lo(w[2]), c2, nmc2)) + hw_exp2(fmaf(bf16_hi(w[2]), c2, nmc2));
-            a3 += hw_exp2(fmaf(bf16_lo(w[3]), c2, nmc2)) + hw_exp2(fmaf(bf16_hi(w[3]), c2, nmc2));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 t = f2_unpack(f2_fma(f2_pack(bf16_lo(w[j]), bf16_hi(w[j])), C2, NM));
+                acc[j] = f2_add(acc[j], f2_pack(hw_exp2(t.x), hw_exp2(t.y)));
+            }
         } else {
-            a0 += hw_exp2(fmaf(__uint_as_float(w[0]), c2, nmc2));
-            a1 += hw_exp2(fmaf(__uint_as_float(w[1]), c2, nmc2));
-            a2 += hw_exp2(fmaf(__uint_as_float(w[2]), c2, nmc2));
-            a3 += hw_exp2(fmaf(__uint_as_float(w[3]), c2, nmc2));
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const float2 t = f2_unpack(f2_fma(f2_pack(__uint_as_float(w[2 * j]), __uint_as_float(w[2 * j + 1])), C2, NM));
+                acc[j] = f2_add(acc[j], f2_pack(hw_exp2(t.x), hw_exp2(t.y)));
+            }
         }
     }
-    float s = warp_sum((a0 + a1) + (a2 + a3));
+    const float2 s0 = f2_unpack(f2_add(acc[0], acc[1])), s1 = f2_unpack(f2_add(acc[2], acc[3]));
+    float s = warp_sum((s0.x + s0.y) + (s1.x + s1.y));
     if (!(s == s) || m == kPosInf) {  // NaN or +inf in the chunk
         if ((threadIdx.x & 31) == 0) raise_error(ws, kErrNonfinite);
     }
@@ -352,21 +393,31 @@ __device__ __forceinline__ void precise_core(const Src& src, bool full, long lon
                                              int lane, const PreciseCtx& P, float4* tot_out,
                                              float4* sub_out) {
     constexpr int SUB = Geo<DT>::kSub;
-    // the block's largest logit
+    // the block's largest logit (bf16: packed maxima; a NaN either comes out as the maximum or
+    // lies outside the table's domain, and the second pass below reports it)
     float m = kNegInf;
     bool nan = false;
     if (full) {
+        if (DT == 1) {
+            const uint4 q0 = src.vec(0);
+            __nv_bfloat162 mx = *reinterpret_cast<const __nv_bfloat162*>(&q0.x);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint4 q = src.vec(i);
-            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+            for (int i = 0; i < 8; ++i) {
+                const uint4 q = i == 0 ? q0 : src.vec(i);
+                const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if (DT == 1) {
-                    const float a = bf16_lo(w[j]), b = bf16_hi(w[j]);
-                    m = fmaxf(m, fmaxf(a, b));
-                    nan |= (a != a) | (b != b);
-                } else {
+                for (int j = 0; j < 4; ++j) mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&w[j]));
+            }
+            const uint32_t mw = *reinterpret_cast<const uint32_t*>(&mx);
+            m = fmaxf(bf16_lo(mw), bf16_hi(mw));
+            nan = (bf16_lo(mw) != bf16_lo(mw)) | (bf16_hi(mw) != bf16_hi(mw));
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint4 q = src.vec(i);
+                const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
                     const float a = __uint_as_float(w[j]);
                     m = fmaxf(m, a);
                     nan |= (a != a);
@@ -383,7 +434,7 @@ __device__ __forceinline__ void precise_core(const Src& src, bool full, long lon
         }
     }
     m = warp_max(m);
-    nan = __any_sync(0xffffffffu, nan);
+    nan = __any_sync(0xffffffffu, nan) || (m != m);
     const float cm = m * (float)P.sc.c;
     const bool ok = !nan && m > kNegInf && cm >= -kMaxScaledLogit && cm <= kMaxScaledLogit;
     if (!ok) {
@@ -400,7 +451,9 @@ __device__ __forceinline__ void precise_core(const Src& src, bool full, long lon
     bool rare = false;  // logits outside the table's domain, added in a second pass below
     const bool direct = DT == 1 && P.tab && P.direct && nref >= kDirectMinRef;
     const bool general_tab = DT == 1 && P.tab && !P.direct;
-    if (full && (direct || general_tab)) {
+    // Table pass without branches: a logit outside the table's domain reads the zero entry
+    // kTabSize and is flagged for the second pass.
+    if (full && direct) {
         const float S = pow2i(-nref);
 #pragma unroll 1
         for (int i = 0; i < 8; ++i) {
@@ -410,20 +463,30 @@ __device__ __forceinline__ void precise_core(const Src& src, bool full, long lon
             for (int j = 0; j < 8; ++j) {
                 const uint32_t b = (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xffffu);
                 const uint32_t off = (b & 0x7fffu) - kTabMagLo;
-                if (off < kTabHalf) {
-                    const float2 e = P.tab[off + ((b & 0x8000u) ? kTabHalf : 0u)];
-                    if (direct) {
-                        acc_biased(acc, dd{f_mul(e.x, S), f_mul(e.y, S)});
-                    } else {
-                        const int n = floor_int(f_mul(bits_to_float<1>(b), P.sc.c2));
-                        const float sc = pow2i(n - nref);
-                        acc_biased(acc, dd{f_mul(e.x, sc), f_mul(e.y, sc)});
-                    }
-                } else {
-                    rare = true;
-                }
+                const bool in = off < kTabHalf;
+                rare |= !in;
+                const float2 e = P.tab[in ? off + (b >> 15) * kTabHalf : (uint32_t)kTabSize];
+                acc_biased(acc, dd{f_mul(e.x, S), f_mul(e.y, S)});
             }
             acc = fast_two_sum(acc.hi, acc.lo);  // keep the low word small
+        }
+    } else if (full && general_tab) {
+#pragma unroll 1
+        for (int i = 0; i < 8; ++i) {
+            const uint4 q = src.vec(i);
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t b = (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xffffu);
+                const uint32_t off = (b & 0x7fffu) - kTabMagLo;
+                const bool in = off < kTabHalf;
+                rare |= !in;
+                const float2 e = P.tab[in ? off + (b >> 15) * kTabHalf : (uint32_t)kTabSize];
+                const int n = floor_int(f_mul(bits_to_float<1>(b), P.sc.c2));
+                const float sc = pow2i(n - nref);
+                acc_biased(acc, dd{f_mul(e.x, sc), f_mul(e.y, sc)});
+            }
+            acc = fast_two_sum(acc.hi, acc.lo);
         }
     } else {
         rare = true;

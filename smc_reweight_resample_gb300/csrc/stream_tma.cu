@@ -28,9 +28,9 @@ constexpr int kRing = kWarp;  // one slot per producer lane
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 constexpr size_t kSmemRing = (size_t)kRing * kChunkBytes;
-constexpr size_t kSmemTab = (size_t)kTabSize * sizeof(float2);
+constexpr size_t kSmemTab = (size_t)kTabAlloc * sizeof(float2);
 constexpr size_t kSmemBytes =
-    kSmemRing + kSmemTab + sizeof(Exp2Table) + 2 * kRing * 8 + kRing * 8 + kRing * 4 + 16;
+    kSmemRing + kSmemTab + sizeof(Exp2Table) + 2 * kRing * 8 + kRing * 16 + kRing * 4 + 16;
 constexpr uint32_t kTagNone = 0xffffffffu;  // slot never loaded
 constexpr uint32_t kTagDone = 0xfffffffeu;  // the slot's claimer has no more chunks
 
@@ -96,6 +96,17 @@ __device__ __forceinline__ bool tag_wait(uint32_t addr, uint32_t k, uint32_t& se
     }
 }
 
+// A slot's record, read after its tag (the tag's acquire orders this load after the producer's
+// store of the record).
+__device__ __forceinline__ int4 ld_meta(uint32_t addr) {
+    int4 v;
+    asm volatile("ld.shared::cta.v4.s32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 // 1-D bulk copy global -> shared, completion counted in bytes on `bar`, with L2 policy `pol`.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
                                           uint32_t bar, uint64_t pol) {
@@ -124,15 +135,15 @@ struct SmemBlock {
 
 // The producer warp: lane j owns slot j. It claims chunks from stripe j of the grid-wide
 // dealing (claim_item) and loads each into its slot once the consumer of the slot's previous
-// chunk has handed the slot back, recording the chunk's index and then tagging the slot with
-// the block-local sequence number k = 32 * round + j. A lane whose stripe is used up tags its
+// chunk has handed the slot back, then writes the slot's record (sequence, row slot and draft
+// count, chunk) and tags the slot with the block-local sequence number k = 32 * round + j. A lane whose stripe is used up tags its
 // slot kTagDone. The lanes poll their slots together (one non-blocking test per lane per pass),
 // so no lane spins alone while the others wait on it. The next claim is made as soon as a chunk
 // is issued, so its latency overlaps the wait for the slot.
 template <int DT>
 __device__ __noinline__ void tma_producer(const StreamParams& p, unsigned char* ring,
                                           uint64_t* full, uint64_t* empty, uint32_t* tag,
-                                          long long* slot_item, unsigned* n_done, int lane) {
+                                          int4* meta, unsigned* n_done, int lane) {
     unsigned* claim = ws_ptr<unsigned>(p.ws, p.L.claim);
     const long long row_bytes = (long long)p.R.V * Geo<DT>::kBytes;
     const uint32_t fb = smem_u32(&full[lane]), eb = smem_u32(&empty[lane]);
@@ -172,14 +183,15 @@ __device__ __noinline__ void tma_producer(const StreamParams& p, unsigned char* 
                            check_ok(p.ws, left > 0 && (bytes & 15u) == 0, -103, left) &&
                            check_ok(p.ws, ((uintptr_t)src & 15u) == 0, -104,
                                     (long long)(uintptr_t)src));
-        slot_item[lane] = it;
-        tag_store(tb, round * kRing + (uint32_t)lane);
         if (c.valid && sane) {
             mbar_arrive_expect_tx(fb, bytes);
             bulk_load(dst, src, bytes, fb, pol);
         } else {
             mbar_arrive(fb);
         }
+        // the slot's record, then its tag
+        meta[lane] = make_int4(c.valid && sane ? c.s : -1, c.slot | (c.ks << 16), c.chunk, 0);
+        tag_store(tb, round * kRing + (uint32_t)lane);
         ++round;
         it = claim_item(claim, lane, kRing, p.items);
         t_last = global_ns();
@@ -200,8 +212,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     Exp2Table* sT = reinterpret_cast<Exp2Table*>(smem + kSmemRing + kSmemTab);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSmemRing + kSmemTab + sizeof(Exp2Table));
     uint64_t* empty = full + kRing;
-    long long* slot_item = reinterpret_cast<long long*>(empty + kRing);
-    uint32_t* tag = reinterpret_cast<uint32_t*>(slot_item + kRing);
+    int4* meta = reinterpret_cast<int4*>(empty + kRing);
+    uint32_t* tag = reinterpret_cast<uint32_t*>(meta + kRing);
     unsigned* next = tag + kRing;
     unsigned* n_done = next + 1;
 
@@ -219,7 +231,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     __syncthreads();
     if (threadIdx.x == 0) griddep_launch_dependents();
     if (warp == 0) {
-        tma_producer<DT>(p, ring, full, empty, tag, slot_item, n_done, lane);
+        tma_producer<DT>(p, ring, full, empty, tag, meta, n_done, lane);
         return;
     }
 
@@ -257,43 +269,38 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             if (lane == 0) raise_error(p.ws, kErrTimeout);
             break;
         }
-        const long long it = *reinterpret_cast<volatile long long*>(&slot_item[slot]);
-        const ChunkRef c = chunk_ref(p, (uint32_t)it);
-        const int x = (lane == 0 && c.valid) ? chunk_token(p, c.s, c.slot, c.ks) : -1;
+        const int4 md = ld_meta(smem_u32(&meta[slot]));
+        const int s = md.x, rs = md.y & 0xffff, ks = md.y >> 16, chunk = md.z;
+        const bool is_draft = rs < 2 * ks && (rs & 1);
         const unsigned char* cbuf = ring + (size_t)slot * kChunkBytes;
-        const bool sane = !c.valid || (check_ok(p.ws, c.chunk >= 0 && c.chunk < p.cpr, -111, c.chunk) &&
-                                       check_ok(p.ws, c.slot >= 0 && c.slot < p.slots, -112, c.slot));
-        if (c.valid && sane) {
-            if (!kPrecise || c.slot != 2 * c.ks) {
+        const bool sane = s < 0 || (check_ok(p.ws, chunk >= 0 && chunk < p.cpr, -111, chunk) &&
+                                    check_ok(p.ws, rs >= 0 && rs < p.slots, -112, rs));
+        if (s >= 0 && sane) {
+            if (!kPrecise || rs != 2 * ks) {
                 uint4 raw[kLoads];
 #pragma unroll
                 for (int v = 0; v < kLoads; ++v)
                     raw[v] = *reinterpret_cast<const uint4*>(cbuf + v * 512 + lane * 16);
-                if (c.chunk == p.cpr - 1) {  // the row's last chunk: mask past V
-                    const long long base = (long long)c.chunk * Geo<DT>::kChunk + lane * Geo<DT>::kPerVec;
+                if (chunk == p.cpr - 1) {  // the row's last chunk: mask past V
+                    const long long base = (long long)chunk * Geo<DT>::kChunk + lane * Geo<DT>::kPerVec;
 #pragma unroll
                     for (int v = 0; v < kLoads; ++v)
                         if (base + v * (Geo<DT>::kChunk / kLoads) >= p.R.V)
                             raw[v] = DT == 0 ? make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u)
                                              : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
                 }
-                const float2 fp = fast_partial<DT>(raw, c.is_draft ? p.sc_d.c2 : p.sc_t.c2, p.ws);
+                const float2 fp = fast_partial<DT>(raw, is_draft ? p.sc_d.c2 : p.sc_t.c2, p.ws);
                 if (lane == 0)
-                    ws_ptr<float2>(p.ws, p.L.fast)[((size_t)c.s * p.slots + c.slot) * p.cpr + c.chunk] = fp;
+                    ws_ptr<float2>(p.ws, p.L.fast)[((size_t)s * p.slots + rs) * p.cpr + chunk] = fp;
             } else {
                 constexpr int SUB = Geo<DT>::kSub;
-                const long long e0 = (long long)c.chunk * Geo<DT>::kChunk + (long long)lane * SUB;
+                const long long e0 = (long long)chunk * Geo<DT>::kChunk + (long long)lane * SUB;
                 const SmemBlock<DT> src{cbuf + lane * 128, lane & 7};
-                float4* tot = ws_ptr<float4>(p.ws, p.L.ddtot) + (size_t)(c.s * 2) * p.cpr + c.chunk;
-                float4* sub = ws_ptr<float4>(p.ws, p.L.ddsub) + ((size_t)(c.s * 2) * p.cpr + c.chunk) * kSubs;
+                float4* tot = ws_ptr<float4>(p.ws, p.L.ddtot) + (size_t)(s * 2) * p.cpr + chunk;
+                float4* sub = ws_ptr<float4>(p.ws, p.L.ddsub) + ((size_t)(s * 2) * p.cpr + chunk) * kSubs;
                 precise_core<DT>(src, e0 + SUB <= p.R.V, e0, p.R.V, lane, P, tot, sub);
             }
         }
-        if (lane == 0 && c.valid && sane && x >= 0)
-            capture_token_logit<DT>(p, c.s, c.slot, c.chunk, x, [&](int off) {
-                return bits_to_float<DT>(DT == 1 ? (uint32_t)reinterpret_cast<const unsigned short*>(cbuf)[off]
-                                                 : reinterpret_cast<const uint32_t*>(cbuf)[off]);
-            });
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
     }

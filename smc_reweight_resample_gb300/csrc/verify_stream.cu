@@ -16,7 +16,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     stream_kernel(const __grid_constant__ StreamParams p) {
     constexpr bool kPrecise = MODE != kModeSD;
     __shared__ Exp2Table sT;
-    __shared__ float2 sTab[(kPrecise && DT == 1) ? kTabSize : 1];
+    __shared__ float2 sTab[(kPrecise && DT == 1) ? kTabAlloc : 1];
     load_exp2_table(p.T, sT);
     PreciseCtx P{p.sc_t, &sT, nullptr, p.ws, p.direct};
     if (kPrecise && DT == 1 && p.use_table) {
@@ -55,12 +55,6 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             float4* tot = ws_ptr<float4>(p.ws, p.L.ddtot) + (size_t)(s * 2) * p.cpr + chunk;
             float4* sub = ws_ptr<float4>(p.ws, p.L.ddsub) + ((size_t)(s * 2) * p.cpr + chunk) * kSubs;
             precise_partials<DT>(rp, p.R.V, p.vec, chunk, lane, P, tot, sub);
-        }
-        if (lane == 0 && slot < 2 * ks) {
-            const int x = chunk_token(p, s, slot, ks);
-            capture_token_logit<DT>(p, s, slot, chunk, x, [&](int off) {
-                return logit_at<DT>(rp, (long long)chunk * Geo<DT>::kChunk + off);
-            });
         }
     }
     __syncthreads();
