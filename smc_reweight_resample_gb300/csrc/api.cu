@@ -239,7 +239,7 @@ extern "C" int smc_ess_resample(float* logw, int G, int N, float ess_threshold,
         return SMCSD_ERR_INVALID_ARG;
     int rc = check_ws(ws, ws_bytes, ws_small_bytes(G));
     if (rc) return rc;
-    ResampleParams p{logw, G, N, ess_threshold, uniforms, ancestors, ess, resampled, ws};
+    ResampleParams p{logw, G, N, ess_threshold, uniforms, ancestors, ess, resampled, ws, exp2_table()};
     return from_cuda(launch_resample(p, (cudaStream_t)stream));
 }
 

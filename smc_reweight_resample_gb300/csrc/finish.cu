@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(kGroupThreads) group_kernel(const __grid_const
         bool res;
         if (N <= kWarp * kResamplePer) {
             int anc_reg[kResamplePer];
-            res = group_resample_small(lw, N, p.ess_threshold, U, anc, ess, rs, p.ws, lane, anc_reg);
+            res = group_resample_small(lw, N, p.ess_threshold, U, anc, ess, rs, p.ws, lane, p.T, anc_reg);
             const int per = (N + kWarp - 1) / kWarp;
 #pragma unroll
             for (int q = 0; q < kResamplePer; ++q)

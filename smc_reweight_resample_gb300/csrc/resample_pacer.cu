@@ -17,7 +17,8 @@ __global__ void __launch_bounds__(128) resample_kernel(const __grid_constant__ R
     if (g >= p.G) return;
     const size_t o = (size_t)g * p.N;
     group_resample(p.logw + o, p.N, p.ess_threshold, __ldg(p.uniforms + g), p.ancestors + o,
-                   p.ess ? p.ess + g : nullptr, p.resampled ? p.resampled + g : nullptr, p.ws, lane);
+                   p.ess ? p.ess + g : nullptr, p.resampled ? p.resampled + g : nullptr, p.ws, lane,
+                   p.T);
 }
 
 __global__ void __launch_bounds__(256) remap_kernel(const __grid_constant__ RemapParams p) {

@@ -37,13 +37,13 @@ __device__ __noinline__ void row_epilogue(const StreamParams& p, const PreciseCt
         const float4* tot = ws_ptr<float4>(p.ws, p.L.ddtot) + (size_t)(s * 2) * p.cpr;
         const float4* sub = ws_ptr<float4>(p.ws, p.L.ddsub) + (size_t)(s * 2) * p.cpr * kSubs;
         const long long row = trow_of(R, s, ks);
-        double lse = 0.0;
+        float lse = 0.0f;
         const int tok = draw_precise_row<DT>(tot, sub, p.cpr, row_ptr<DT>(R.tgt, row, R.V), R.V, P,
                                              __ldg(p.uniforms + s), lane, &lse);
         if (lane == 0) {
             if (tok < 0) raise_error(p.ws, kErrNonfinite);
             p.bonus_token[s] = tok < 0 ? 0 : tok;
-            if (p.lse_tgt) p.lse_tgt[row] = (float)lse;
+            if (p.lse_tgt) p.lse_tgt[row] = lse;
         }
         return;
     }
@@ -57,41 +57,46 @@ __device__ __noinline__ void row_epilogue(const StreamParams& p, const PreciseCt
             zx = is_draft ? logit_at<DT>(row_ptr<DT>(R.drf, drow_of(R, s, k), R.V), x)
                           : logit_at<DT>(row_ptr<DT>(R.tgt, trow_of(R, s, k), R.V), x);
     }
-    const double L = row_lse_fast(ws_ptr<float2>(p.ws, p.L.fast) + r * p.cpr, p.cpr,
-                                  is_draft ? p.sc_d : p.sc_t, lane);
+    const dd L = row_lse_fast(ws_ptr<float2>(p.ws, p.L.fast) + r * p.cpr, p.cpr,
+                              is_draft ? p.sc_d : p.sc_t, lane);
     if (lane == 0) {
         if (slot < 2 * ks) ws_ptr<float>(p.ws, p.L.zsel)[r] = zx;
-        if (!(L == L)) raise_error(p.ws, kErrNonfinite);  // a row without mass
-        ws_ptr<double>(p.ws, p.L.rowL)[r] = L;
+        if (!(L.hi == L.hi)) raise_error(p.ws, kErrNonfinite);  // a row without mass
+        ws_ptr<float2>(p.ws, p.L.rowL)[r] = make_float2(L.hi, L.lo);
+        const float Lf = f_add(L.hi, L.lo);
         if (is_draft) {
-            if (p.lse_drf) p.lse_drf[drow_of(R, s, k)] = (float)L;
+            if (p.lse_drf) p.lse_drf[drow_of(R, s, k)] = Lf;
         } else if (p.lse_tgt) {
-            p.lse_tgt[trow_of(R, s, k)] = (float)L;
+            p.lse_tgt[trow_of(R, s, k)] = Lf;
         }
     }
 }
 
-// log p_k(x_k) - log q_k(x_k) at position k of sequence s, from the row normalisers and the
-// logits recorded at the draft token. False (with an error raised) if the token is out of range.
-__device__ __forceinline__ bool log_ratio(const StreamParams& p, int s, int k, double& ell) {
+// log p_k(x_k) - log q_k(x_k) at position k of sequence s, as a double-float, from the row
+// normalisers and the logits recorded at the draft token. False (with an error raised) if the
+// token is out of range.
+__device__ __forceinline__ bool log_ratio(const StreamParams& p, int s, int k, dd& ell) {
     const Rows& R = p.R;
     const int x = __ldg(R.toks + drow_of(R, s, k));
     const size_t r = (size_t)s * p.slots + 2 * k;
-    const double* rowL = ws_ptr<double>(p.ws, p.L.rowL);
+    const float2* rowL = ws_ptr<float2>(p.ws, p.L.rowL);
     const float* zsel = ws_ptr<float>(p.ws, p.L.zsel);
-    const double Lt = __ldcg(rowL + r), Ld = __ldcg(rowL + r + 1);
+    const float2 Lt = __ldcg(rowL + r), Ld = __ldcg(rowL + r + 1);
     const float zt = __ldcg(zsel + r), zd = __ldcg(zsel + r + 1);
-    ell = 0.0;
+    ell = dd{0.0f, 0.0f};
     if (x < 0 || x >= R.V) {
         raise_error(p.ws, kErrRange);
         return false;
     }
-    ell = (p.sc_t.c * (double)zt - Lt) - (p.sc_d.c * (double)zd - Ld);
+    const dd lt = dd_sub(dd_mul_f(dd{p.sc_t.c_hi, p.sc_t.c_lo}, zt), dd{Lt.x, Lt.y});
+    const dd ld = dd_sub(dd_mul_f(dd{p.sc_d.c_hi, p.sc_d.c_lo}, zd), dd{Ld.x, Ld.y});
+    ell = dd_sub(lt, ld);
     return true;
 }
 
 // SD: the ratio tests min(1, p/q) in position order, the acceptance length and the hand-off of
-// the row (pair) to draw the final token from.
+// the row (pair) to draw the final token from. Position k is accepted iff u_k < exp(min(0, l_k)),
+// with the exponential in double-float.
 static __device__ __noinline__ void sd_seq_epilogue(const StreamParams& p, int s, int ks, int lane) {
     const Rows& R = p.R;
     const float* u = p.uniforms + (size_t)s * (R.K + 1);
@@ -100,10 +105,16 @@ static __device__ __noinline__ void sd_seq_epilogue(const StreamParams& p, int s
         const int k = k0 + lane;
         bool rej = false;
         if (k < ks) {
-            double ell;
+            dd ell;
             const bool ok = log_ratio(p, s, k, ell);
-            const double a = exp(ell < 0.0 ? ell : 0.0);  // min(1, p/q)
-            rej = !ok || !((double)__ldg(u + k) < a);
+            const float uk = __ldg(u + k);
+            if (!ok || !(ell.hi == ell.hi)) {
+                rej = true;
+            } else if (ell.hi < 0.0f) {
+                const ddx e = exp_split(ell, p.T);
+                const float sc = pow2i(e.n);
+                rej = !dd_gt(dd{f_mul(e.hi, sc), f_mul(e.lo, sc)}, dd{uk, 0.0f});
+            }  // l_k >= 0: the ratio is at least 1 > u
         }
         const unsigned b = __ballot_sync(0xffffffffu, rej);
         if (b && acc == ks) acc = k0 + __ffs(b) - 1;
@@ -118,15 +129,18 @@ static __device__ __noinline__ void sd_seq_epilogue(const StreamParams& p, int s
     }
 }
 
-// SMC: log-weight update sum_k log pi_k(x_k) - log q_k(x_k) of particle s.
+// SMC: log-weight update sum_k log pi_k(x_k) - log q_k(x_k) of particle s (double-float sums).
 static __device__ __noinline__ void smc_particle_epilogue(const StreamParams& p, int s, int lane) {
-    double inc = 0.0;
+    dd inc{0.0f, 0.0f};
     for (int k = lane; k < p.R.K; k += kWarp) {
-        double ell;
-        if (log_ratio(p, s, k, ell)) inc += ell;
+        dd ell;
+        if (log_ratio(p, s, k, ell)) inc = dd_add(inc, ell);
     }
-    inc = warp_sum_d(inc);
-    if (lane == 0) p.logw[s] = (float)((double)__ldcg(p.logw + s) + inc);
+    inc = warp_sum_dd(inc);
+    if (lane == 0) {
+        const dd lw = dd_add(dd{__ldcg(p.logw + s), 0.0f}, inc);
+        p.logw[s] = f_add(lw.hi, lw.lo);
+    }
 }
 
 // Page-table rows of one group after resampling, by all threads of a block: row j of the output

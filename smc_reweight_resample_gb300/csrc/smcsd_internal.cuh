@@ -88,7 +88,7 @@ struct WsLayout {
     size_t rtot;       // float4 [S * cpr]              residual chunk totals (SD)
     size_t rsub;       // float4 [S * cpr * kSubs]      residual lane-block partials (SD)
     size_t seq;        // SeqState [S]
-    size_t rowL;       // double [S * (2K+1)]  row normalisers log sum_i exp(c z_i)
+    size_t rowL;       // float2 [S * (2K+1)] row normalisers log sum_i exp(c z_i), double-float
     size_t zsel;       // float  [S * (2K+1)]  logit of the row at its draft token
     size_t tab;        // cached exp table: 4 tag words + 4608 float2 (see setup_exp_table)
     size_t total;

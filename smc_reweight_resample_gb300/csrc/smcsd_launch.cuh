@@ -72,6 +72,7 @@ struct ResampleParams {
     float* ess;
     int32_t* resampled;
     void* ws;
+    Exp2Table T;
 };
 
 struct RemapParams {

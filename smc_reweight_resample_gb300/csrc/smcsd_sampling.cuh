@@ -306,8 +306,9 @@ __device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsig
 }
 
 // Fast partial of one chunk: {m, sum_i 2^(z_i c2 - fl(m c2))} with m the chunk's largest logit
-// (raw, before scaling; c > 0 keeps the order). An all-masked chunk gives {-inf, 0}. The maximum
-// runs as four independent chains; the exponent arguments and the sums as float pairs.
+// (raw, before scaling; c > 0 keeps the order), up to the rounding of the final rescaling. An
+// all-masked chunk gives {-inf, 0}. The maximum runs as four independent chains; the exponent
+// arguments and the sums as float pairs.
 template <int DT>
 __device__ __forceinline__ float2 fast_partial(const uint4 (&raw)[kLoads], float c2, void* ws) {
     float m;
@@ -338,8 +339,31 @@ __device__ __forceinline__ float2 fast_partial(const uint4 (&raw)[kLoads], float
         }
         m = fmaxf(fmaxf(mf[0], mf[1]), fmaxf(mf[2], mf[3]));
     }
-    m = warp_max(m);
-    if (m == kNegInf) {
+    // Each lane sums relative to its own maximum, so the exponentials need not wait for the
+    // warp's; the lanes' sums are rescaled to the chunk maximum at the end.
+    const bool live = m > kNegInf;
+    const float q = live ? m * c2 : 0.0f;  // fl(m_lane c2)
+    const unsigned long long C2 = f2_pack(c2, c2), NQ = f2_pack(-q, -q);
+    unsigned long long acc[4] = {0ull, 0ull, 0ull, 0ull};  // (+0.0f, +0.0f) pairs
+#pragma unroll
+    for (int v = 0; v < kLoads; ++v) {
+        const uint32_t w[4] = {raw[v].x, raw[v].y, raw[v].z, raw[v].w};
+        if (DT == 1) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 t = f2_unpack(f2_fma(f2_pack(bf16_lo(w[j]), bf16_hi(w[j])), C2, NQ));
+                acc[j] = f2_add(acc[j], f2_pack(hw_exp2(t.x), hw_exp2(t.y)));
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const float2 t = f2_unpack(f2_fma(f2_pack(__uint_as_float(w[2 * j]), __uint_as_float(w[2 * j + 1])), C2, NQ));
+                acc[j] = f2_add(acc[j], f2_pack(hw_exp2(t.x), hw_exp2(t.y)));
+            }
+        }
+    }
+    const float M = warp_max(m);
+    if (M == kNegInf) {
         bool nan = false;
 #pragma unroll
         for (int v = 0; v < kLoads; ++v) {
@@ -355,32 +379,14 @@ __device__ __forceinline__ float2 fast_partial(const uint4 (&raw)[kLoads], float
         if (__any_sync(0xffffffffu, nan) && (threadIdx.x & 31) == 0) raise_error(ws, kErrNonfinite);
         return make_float2(kNegInf, 0.0f);
     }
-    const float nmc2 = -(m * c2);
-    const unsigned long long C2 = f2_pack(c2, c2), NM = f2_pack(nmc2, nmc2);
-    unsigned long long acc[4] = {0ull, 0ull, 0ull, 0ull};  // (+0.0f, +0.0f) pairs
-#pragma unroll
-    for (int v = 0; v < kLoads; ++v) {
-        const uint32_t w[4] = {raw[v].x, raw[v].y, raw[v].z, raw[v].w};
-        if (DT == 1) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float2 t = f2_unpack(f2_fma(f2_pack(bf16_lo(w[j]), bf16_hi(w[j])), C2, NM));
-                acc[j] = f2_add(acc[j], f2_pack(hw_exp2(t.x), hw_exp2(t.y)));
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const float2 t = f2_unpack(f2_fma(f2_pack(__uint_as_float(w[2 * j]), __uint_as_float(w[2 * j + 1])), C2, NM));
-                acc[j] = f2_add(acc[j], f2_pack(hw_exp2(t.x), hw_exp2(t.y)));
-            }
-        }
-    }
     const float2 s0 = f2_unpack(f2_add(acc[0], acc[1])), s1 = f2_unpack(f2_add(acc[2], acc[3]));
-    float s = warp_sum((s0.x + s0.y) + (s1.x + s1.y));
-    if (!(s == s) || m == kPosInf) {  // NaN or +inf in the chunk
+    const float sl = (s0.x + s0.y) + (s1.x + s1.y);
+    const float t = live ? sl * hw_exp2(q - M * c2) : 0.0f;
+    const float s = warp_sum(t);
+    if (!(s == s) || M == kPosInf) {  // NaN or +inf in the chunk
         if ((threadIdx.x & 31) == 0) raise_error(ws, kErrNonfinite);
     }
-    return make_float2(m, s);
+    return make_float2(M, s);
 }
 
 // Precise partials of one chunk of a row that will be sampled. Lane l stores the double-float
@@ -435,7 +441,7 @@ __device__ __forceinline__ void precise_core(const Src& src, bool full, long lon
     }
     m = warp_max(m);
     nan = __any_sync(0xffffffffu, nan) || (m != m);
-    const float cm = m * (float)P.sc.c;
+    const float cm = m * P.sc.c_hi;
     const bool ok = !nan && m > kNegInf && cm >= -kMaxScaledLogit && cm <= kMaxScaledLogit;
     if (!ok) {
         // NaN anywhere, +inf, or a scaled logit above the supported range is an error; a chunk
@@ -535,9 +541,11 @@ __device__ __forceinline__ void precise_partials(const void* row, int V, bool ve
 // row normalisers from fast partials
 // ------------------------------------------------------------------------------------------
 
-// Natural-log normaliser log sum_i exp(c z_i) of one row from its cpr fast partials, on every
-// lane (NaN for a row without mass). The partials' loads are all in flight together.
-__device__ __forceinline__ double row_lse_fast(const float2* part, int cpr, const Scale& sc, int lane) {
+// Natural-log normaliser log sum_i exp(c z_i) of one row from its cpr fast partials, as a
+// double-float on every lane (hi = NaN for a row without mass): c M exactly, plus the float
+// log of the rescaled sum and the residual of fl(M c2). The partials' loads are all in flight
+// together.
+__device__ __forceinline__ dd row_lse_fast(const float2* part, int cpr, const Scale& sc, int lane) {
     float mq = kNegInf, s = 0.0f, M = kNegInf;  // running fl(m c2) of the lane's largest chunk, its sum, max m
     for (int c0 = 0; c0 < cpr; c0 += 4 * kWarp) {
         float2 v[4];
@@ -564,9 +572,10 @@ __device__ __forceinline__ double row_lse_fast(const float2* part, int cpr, cons
     const float Q = Mb * sc.c2;
     const float t = (mq == kNegInf) ? 0.0f : s * hw_exp2(mq - Q);
     const float Ssum = warp_sum(t);
-    if (Mb == kNegInf || !(Ssum > 0.0f)) return __longlong_as_double(0x7ff8000000000000ll);
+    if (Mb == kNegInf || !(Ssum > 0.0f)) return dd{__int_as_float(0x7fc00000), 0.0f};
     const float rQ = fmaf(Mb, sc.c2, -Q);  // exact residual of fl(M c2)
-    return sc.c * (double)Mb + log((double)Ssum) - (double)rQ * 0.69314718055994530942;
+    const dd cM = dd_mul_f(dd{sc.c_hi, sc.c_lo}, Mb);
+    return dd_add(cM, two_sum(logf(Ssum), -rQ * SMCSD_LN2_HI));
 }
 
 // ------------------------------------------------------------------------------------------
@@ -584,14 +593,14 @@ __device__ __forceinline__ dd part_value(float4 p, int N) {
 // [cpr] and lane-block partials `sub` [cpr * kSubs] describe the weights, rescanning one lane
 // block with `block_weights(chunk, sub, lane, N, w[PL])` (PL = kSub / 32 weights per lane, in
 // units of 2^N, reproducing the partials exactly). Returns the token on every lane (-1 if the
-// row has no mass). If `lse` is given it receives log(sum_j w_j) + N ln 2. Lane l reads the
+// row has no mass). If `lse` is given it receives log(sum_j w_j) + N ln 2 (in float). Lane l reads the
 // contiguous chunk totals [l*cpl, l*cpl + cpl) once (kept in registers up to kDrawCache per
 // lane) and serves both the common exponent and the chunk-level walk from them.
 constexpr int kDrawCache = 4;
 template <int PL, typename BlockFn>
 __device__ int draw_inverse_cdf(const float4* tot, const float4* sub, int cpr, int chunk_elems,
                                 int sub_elems, float u, int lane, BlockFn block_weights,
-                                double* lse) {
+                                float* lse) {
     const int cpl = (cpr + kWarp - 1) / kWarp;
     const int c_begin = min(lane * cpl, cpr), c_end = min(c_begin + cpl, cpr);
     const bool cached = cpl <= kDrawCache;
@@ -624,7 +633,7 @@ __device__ int draw_inverse_cdf(const float4* tot, const float4* sub, int cpr, i
     const dd excl = warp_exclusive_scan_dd(loc, lane);
     const dd incl = dd_add(excl, loc);
     const dd R{__shfl_sync(0xffffffffu, incl.hi, 31), __shfl_sync(0xffffffffu, incl.lo, 31)};
-    if (lse) *lse = log(dd_to_double(R)) + (double)N * 0.69314718055994530942;
+    if (lse) *lse = f_add(f_mul((float)N, SMCSD_LN2_HI), f_add(logf(R.hi), f_div(R.lo, R.hi)));
     const dd target = dd_mul_f(R, u);
 
     bool has = loc.hi > 0.0f && dd_gt(incl, target);
@@ -763,7 +772,7 @@ __device__ __forceinline__ dd row_total(const float4* tot, int cpr, int N, int l
 template <int DT>
 __device__ __forceinline__ int draw_precise_row(const float4* tot, const float4* sub, int cpr,
                                                 const void* row, int V, const PreciseCtx& P,
-                                                float u, int lane, double* lse) {
+                                                float u, int lane, float* lse) {
     PreciseBlock<DT> fn{row, V, P};
     return draw_inverse_cdf<PreciseBlock<DT>::PL>(tot, sub, cpr, Geo<DT>::kChunk, Geo<DT>::kSub,
                                                   u, lane, fn, lse);
@@ -786,21 +795,24 @@ __device__ __forceinline__ int children_below(double C, double U, int N) {
 }
 
 // Resampling of a group of at most kWarp * kResamplePer particles with every weight computed
-// once and held in registers (lane l holds particles l*per .. l*per+per-1). The ancestor of
-// child j is the number of particles i with C_i <= v_j = (j + U) / N (C is nondecreasing below
-// 1 and C_{N-1} = 1 > v_j), found by a branch-free binary search over the C_i in the lanes'
-// registers that compares the bit patterns of the nonnegative doubles, which order like the
-// values. The ancestors of the lane's children are also left in anc_reg (N when not resampled).
+// once and held in registers (lane l holds particles l*per .. l*per+per-1), in double-float
+// arithmetic on the FP32 pipes (about 2^-44 relative; this GPU's FP64 rate is far lower): the
+// weights w_i = exp(logw_i - max) from the double-float exp, ESS = W^2 / W2, the CDF
+// C_i = (prefix sum)/W with C_{N-1} = 1, the points v_j = (j + U)/N. The ancestor of child j is
+// the number of particles i with C_i <= v_j (C is nondecreasing below 1 and C_{N-1} = 1 > v_j),
+// found by a branch-free binary search over the C_i in the lanes' registers. The ancestors of
+// the lane's children are also left in anc_reg (identity when not resampled).
 constexpr int kResamplePer = 4;
 
 // Value of register q of lane `src`, for a per-lane (src, q); `per` registers are live.
-__device__ __forceinline__ long long shfl_pick(const long long (&v)[kResamplePer], int per, int src, int q) {
-    long long r = 0;
+__device__ __forceinline__ dd shfl_pick_dd(const dd (&v)[kResamplePer], int per, int src, int q) {
+    dd r{0.0f, 0.0f};
 #pragma unroll
     for (int q2 = 0; q2 < kResamplePer; ++q2) {
         if (q2 < per) {
-            const long long t = __shfl_sync(0xffffffffu, v[q2], src);
-            if (q2 == q) r = t;
+            const float hi = __shfl_sync(0xffffffffu, v[q2].hi, src);
+            const float lo = __shfl_sync(0xffffffffu, v[q2].lo, src);
+            if (q2 == q) r = dd{hi, lo};
         }
     }
     return r;
@@ -808,7 +820,8 @@ __device__ __forceinline__ long long shfl_pick(const long long (&v)[kResamplePer
 
 __device__ __forceinline__ bool group_resample_small(float* logw, int N, float thr, float U,
                                                      int32_t* anc, float* ess_out, int32_t* res_out,
-                                                     void* ws, int lane, int (&anc_reg)[kResamplePer]) {
+                                                     void* ws, int lane, const Exp2Table& T,
+                                                     int (&anc_reg)[kResamplePer]) {
     const int per = (N + kWarp - 1) / kWarp;
     const int i0 = min(lane * per, N), i1 = min(i0 + per, N);
 #pragma unroll
@@ -825,47 +838,49 @@ __device__ __forceinline__ bool group_resample_small(float* logw, int N, float t
             m = fmaxf(m, v[q]);
         }
     }
-    const double M = (double)warp_max(m);
-    bad = __any_sync(0xffffffffu, bad) || M == -__builtin_huge_val();
+    const float M = warp_max(m);
+    bad = __any_sync(0xffffffffu, bad) || M == kNegInf;
     if (bad) {
         if (lane == 0) raise_error(ws, kErrNonfinite);
         for (int j = lane; j < N; j += kWarp) anc[j] = j;
         if (lane == 0 && res_out) *res_out = 0;
         return false;
     }
-    double w[kResamplePer];
-    double loc = 0.0, loc2 = 0.0;
+    dd w[kResamplePer];
+    dd loc{0.0f, 0.0f}, loc2{0.0f, 0.0f};
 #pragma unroll
     for (int q = 0; q < kResamplePer; ++q) {
-        w[q] = 0.0;
-        if (q < per) {  // (uniform) every double operation counts: keep them to the live ones
-            if (i0 + q < i1) w[q] = exp((double)v[q] - M);
-            loc += w[q];
-            loc2 += w[q] * w[q];
+        w[q] = dd{0.0f, 0.0f};
+        if (q < per && i0 + q < i1 && v[q] > kNegInf) {
+            const ddx e = exp_split(two_sum(v[q], -M), T);  // logw_i - max, exact as a double-float
+            const float sc = pow2i(e.n);
+            w[q] = dd{f_mul(e.hi, sc), f_mul(e.lo, sc)};
+            loc = dd_add(loc, w[q]);
+            loc2 = dd_add(loc2, dd_mul(w[q], w[q]));
         }
     }
-    const double W = warp_sum_d(loc), W2 = warp_sum_d(loc2);
-    const double ess = W * W / W2;
-    const bool res = ess < (double)thr;
+    const dd W = warp_sum_dd(loc), W2 = warp_sum_dd(loc2);
+    const dd ess = dd_mul(dd_mul(W, W), dd_recip(W2));
+    const bool res = dd_gt(dd{thr, 0.0f}, ess);  // ESS < threshold
     if (lane == 0) {
-        if (ess_out) *ess_out = (float)ess;
+        if (ess_out) *ess_out = f_add(ess.hi, ess.lo);
         if (res_out) *res_out = res ? 1 : 0;
     }
     if (!res) {
         for (int j = lane; j < N; j += kWarp) anc[j] = j;
         return false;
     }
-    long long cb[kResamplePer], vb[kResamplePer];
-    double r = warp_exclusive_scan_d(loc, lane);
-    const double Ud = (double)U;
+    const dd rW = dd_recip(W), rN = dd_recip(dd{(float)N, 0.0f});
+    dd C[kResamplePer], Vj[kResamplePer];
+    dd r = warp_exclusive_scan_dd(loc, lane);
 #pragma unroll
     for (int q = 0; q < kResamplePer; ++q) {
-        cb[q] = vb[q] = 0;
+        C[q] = Vj[q] = dd{0.0f, 0.0f};
         if (q < per) {
-            r += w[q];
+            r = dd_add(r, w[q]);
             const int i = i0 + q;
-            cb[q] = __double_as_longlong(i == N - 1 ? 1.0 : r / W);
-            vb[q] = __double_as_longlong(((double)i + Ud) / (double)N);
+            C[q] = i == N - 1 ? dd{1.0f, 0.0f} : dd_mul(r, rW);
+            Vj[q] = dd_mul(two_sum((float)i, U), rN);
         }
     }
     int top = 1;
@@ -877,8 +892,8 @@ __device__ __forceinline__ bool group_resample_small(float* logw, int N, float t
             if (q < per) {
                 const int probe = cnt[q] + step - 1;
                 const int pc = min(probe, N - 1);
-                const long long c = shfl_pick(cb, per, pc / per, pc - (pc / per) * per);
-                if (probe < N && c <= vb[q]) cnt[q] += step;
+                const dd c = shfl_pick_dd(C, per, pc / per, pc - (pc / per) * per);
+                if (probe < N && !dd_gt(c, Vj[q])) cnt[q] += step;
             }
         }
     }
@@ -977,10 +992,11 @@ static __device__ __noinline__ bool group_resample_general(float* logw, int N, f
 // logw [N] of one group (float, in/out). Writes ancestors [N], *ess_out, *res_out (if given).
 // Returns whether the group was resampled (on every lane).
 __device__ __forceinline__ bool group_resample(float* logw, int N, float thr, float U, int32_t* anc,
-                                               float* ess_out, int32_t* res_out, void* ws, int lane) {
+                                               float* ess_out, int32_t* res_out, void* ws, int lane,
+                                               const Exp2Table& T) {
     if (N <= kWarp * kResamplePer) {
         int anc_reg[kResamplePer];
-        return group_resample_small(logw, N, thr, U, anc, ess_out, res_out, ws, lane, anc_reg);
+        return group_resample_small(logw, N, thr, U, anc, ess_out, res_out, ws, lane, T, anc_reg);
     }
     return group_resample_general(logw, N, thr, U, anc, ess_out, res_out, ws, lane);
 }

@@ -3,17 +3,16 @@
 // One block per SM: a producer warp that moves 4 KB chunks of logits from HBM into a ring of
 // kRing = 32 shared-memory slots with the bulk-copy engine (cp.async.bulk, completion counted on
 // one mbarrier per slot; lane j of the producer fills slot j), and kTmaConsumers consumer warps
-// that take the slots in the order they were filled from a shared counter, wait for theirs,
-// compute the chunk's partial (fast or precise, smcsd_sampling.cuh) from shared memory, hand
-// the slot back (a second mbarrier per slot) and count the chunk for its row; the last chunk of
-// a row runs the row's epilogue and so on up (smcsd_epilogue.cuh). The producer runs up to
-// kRing chunks (128 KB) ahead, so the consumers never wait on HBM latency, and every logit
-// still crosses HBM exactly once.
+// that take the slots in the order they were filled from a shared counter, wait for theirs and
+// compute the chunk's partial (fast or precise, smcsd_sampling.cuh) into the workspace, where
+// the finishing pass (finish.cu) picks the partials up. A fast chunk is copied into registers
+// and its slot handed back (a second mbarrier per slot) before the arithmetic, so that nearly
+// the whole ring stays in flight; a precise chunk, read twice, keeps its slot until done. Every
+// logit crosses HBM exactly once.
 //
 // Chunks (sequence-major order) are dealt dynamically: producer lane j of every block claims the
-// next chunk of stripe j (chunks j, j+32, j+64, ...) from a grid-wide counter. A block that is
-// busy with an epilogue simply claims fewer chunks, and the last chunk of a row, whose warp runs
-// the row's epilogue, lands on whichever block reaches it, so no block collects the epilogues.
+// next chunk of stripe j (chunks j, j+32, j+64, ...) from a grid-wide counter, so the blocks stay
+// balanced whatever the mix of fast and precise chunks they draw.
 //
 // Every wait is bounded (about 2 s of wall time): a wait that runs out records
 // SMCSD_ERR_TIMEOUT in the workspace and the warp leaves; the producer, before it leaves,
@@ -22,7 +21,7 @@
 
 namespace smcsd {
 
-constexpr int kTmaConsumers = 16;
+constexpr int kTmaConsumers = 18;
 constexpr int kTmaThreads = (kTmaConsumers + 1) * kWarp;
 constexpr int kRing = kWarp;  // one slot per producer lane
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
@@ -30,7 +29,7 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 constexpr size_t kSmemRing = (size_t)kRing * kChunkBytes;
 constexpr size_t kSmemTab = (size_t)kTabAlloc * sizeof(float2);
 constexpr size_t kSmemBytes =
-    kSmemRing + kSmemTab + sizeof(Exp2Table) + 2 * kRing * 8 + kRing * 16 + kRing * 4 + 16;
+    kSmemRing + kSmemTab + sizeof(Exp2Table) + 2 * kRing * 8 + kRing * 8 + 16;
 constexpr uint32_t kTagNone = 0xffffffffu;  // slot never loaded
 constexpr uint32_t kTagDone = 0xfffffffeu;  // the slot's claimer has no more chunks
 
@@ -47,10 +46,31 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// Relaxed arrivals: they order nothing, so they never wait for this warp's outstanding global
+// accesses (claims, partial stores). Used where nothing written before the arrival is read by
+// the waiting side (the data comes through the bulk copy or has already been read out).
+__device__ __forceinline__ void mbar_arrive_expect_tx_relaxed(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.relaxed.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_relaxed(uint32_t bar) {
+    asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Non-blocking test of the phase of `parity` (try_wait may suspend the thread for a while).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
         " selp.u32 %0, 1, 0, p;\n}"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
@@ -70,41 +90,45 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
         if (global_ns() - t0 > kWaitLimitNs) return false;
     return true;
 }
-// Slot tags: the producer writes the index k of the chunk it is about to load into a slot before
-// it arms the slot's barrier. A consumer holding chunk k waits for the tag first, so that the
-// barrier it then waits on is known to be in the phase of chunk k: a parity wait alone cannot
-// tell that phase from the one two loads earlier, and the consumers take chunks from a shared
-// counter, so a consumer can reach a slot before the previous chunk of that slot has landed.
-__device__ __forceinline__ void tag_store(uint32_t addr, uint32_t k) {
-    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(addr), "r"(k) : "memory");
+// Slot tags: one 64-bit word per slot, written by the producer once the slot's chunk is on its
+// way: the block-local sequence number k of the load in the high half, the chunk's index in the
+// low half. A consumer holding k waits for its tag first, so that the full barrier it then waits
+// on is known to be in the phase of chunk k: a parity wait alone cannot tell that phase from the
+// one two loads earlier, and the consumers take the slots from a shared counter, so a consumer
+// can reach a slot before the previous chunk of that slot has landed. An aligned 8-byte access
+// is single-copy atomic, so the chunk index comes with the tag and neither side needs a fence.
+__device__ __forceinline__ void tag_store(uint32_t addr, uint32_t k, uint32_t item) {
+    const unsigned long long v = ((unsigned long long)k << 32) | item;
+    asm volatile("st.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
 }
-__device__ __forceinline__ uint32_t tag_load(uint32_t addr) {
-    uint32_t v;
-    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+__device__ __forceinline__ unsigned long long tag_load(uint32_t addr) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.cta.shared::cta.b64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
     return v;
 }
-// Wait (at most kWaitLimitNs) until the tag at `addr` reads k or kTagDone; the tag seen is
+// Wait (at most kWaitLimitNs) until the tag at `addr` reads k or kTagDone; the tag word seen is
 // left in `seen`.
-__device__ __forceinline__ bool tag_wait(uint32_t addr, uint32_t k, uint32_t& seen) {
+__device__ __forceinline__ bool tag_wait(uint32_t addr, uint32_t k, unsigned long long& seen) {
     seen = tag_load(addr);
-    if (seen == k || seen == kTagDone) return true;
+    uint32_t hi = (uint32_t)(seen >> 32);
+    if (hi == k || hi == kTagDone) return true;
     const unsigned long long t0 = global_ns();
     for (;;) {
+        __nanosleep(32);
         seen = tag_load(addr);
-        if (seen == k || seen == kTagDone) return true;
+        hi = (uint32_t)(seen >> 32);
+        if (hi == k || hi == kTagDone) return true;
         if (global_ns() - t0 > kWaitLimitNs) return false;
     }
 }
 
-// A slot's record, read after its tag (the tag's acquire orders this load after the producer's
-// store of the record).
-__device__ __forceinline__ int4 ld_meta(uint32_t addr) {
-    int4 v;
-    asm volatile("ld.shared::cta.v4.s32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr)
-                 : "memory");
-    return v;
+// Makes every word of `raw` an input of an (empty) instruction: what follows in program order
+// is issued only after all of them have arrived in registers.
+__device__ __forceinline__ void consume_all(const uint4 (&raw)[kLoads]) {
+    uint32_t x = 0;
+#pragma unroll
+    for (int v = 0; v < kLoads; ++v) x ^= raw[v].x ^ raw[v].y ^ raw[v].z ^ raw[v].w;
+    asm volatile("" ::"r"(x) : "memory");
 }
 
 // 1-D bulk copy global -> shared, completion counted in bytes on `bar`, with L2 policy `pol`.
@@ -138,25 +162,33 @@ struct SmemBlock {
 // chunk has handed the slot back, then writes the slot's record (sequence, row slot and draft
 // count, chunk) and tags the slot with the block-local sequence number k = 32 * round + j. A lane whose stripe is used up tags its
 // slot kTagDone. The lanes poll their slots together (one non-blocking test per lane per pass),
-// so no lane spins alone while the others wait on it. The next claim is made as soon as a chunk
-// is issued, so its latency overlaps the wait for the slot.
+// so no lane spins alone while the others wait on it; the test does not block. Each lane keeps
+// its next two chunks claimed, so a claim's latency is hidden behind a whole refill.
 template <int DT>
 __device__ __noinline__ void tma_producer(const StreamParams& p, unsigned char* ring,
-                                          uint64_t* full, uint64_t* empty, uint32_t* tag,
-                                          int4* meta, unsigned* n_done, int lane) {
+                                          uint64_t* full, uint64_t* empty,
+                                          unsigned long long* tag, unsigned* n_done, int lane) {
     unsigned* claim = ws_ptr<unsigned>(p.ws, p.L.claim);
     const long long row_bytes = (long long)p.R.V * Geo<DT>::kBytes;
     const uint32_t fb = smem_u32(&full[lane]), eb = smem_u32(&empty[lane]);
     const uint32_t tb = smem_u32(&tag[lane]);
     const uint32_t dst = smem_u32(ring + (size_t)lane * kChunkBytes);
     const uint64_t pol = l2_evict_first();
+    // two claims ahead: `it` is the lane's next chunk, `it_next` the one after, whose claim is in
+    // flight while `it` waits for the slot
     long long it = claim_item(claim, lane, kRing, p.items);
+    long long it_next = claim_item(claim, lane, kRing, p.items);
     uint32_t round = 0;
     bool done = false;
     unsigned long long t_last = global_ns();
+    bool moved = true;
     while (__any_sync(0xffffffffu, !done)) {
+        // a pass in which no lane could refill its slot backs off briefly instead of spinning on
+        // the issue slots the consumer warps of this sub-partition need
+        if (!__any_sync(0xffffffffu, moved)) __nanosleep(200);
+        moved = false;
         if (done) continue;
-        if (round > 0 && !mbar_try_wait(eb, (round - 1) & 1u)) {
+        if (round > 0 && !mbar_test_wait(eb, (round - 1) & 1u)) {
             if (global_ns() - t_last > kWaitLimitNs) {
                 raise_error(p.ws, kErrTimeout);
                 it = -1;  // give the slot up below so that its consumers stop
@@ -164,9 +196,10 @@ __device__ __noinline__ void tma_producer(const StreamParams& p, unsigned char* 
                 continue;
             }
         }
+        moved = true;
         if (it < 0) {
             atomicAdd(n_done, 1u);
-            tag_store(tb, kTagDone);
+            tag_store(tb, kTagDone, 0u);
             done = true;
             continue;
         }
@@ -184,16 +217,15 @@ __device__ __noinline__ void tma_producer(const StreamParams& p, unsigned char* 
                            check_ok(p.ws, ((uintptr_t)src & 15u) == 0, -104,
                                     (long long)(uintptr_t)src));
         if (c.valid && sane) {
-            mbar_arrive_expect_tx(fb, bytes);
+            mbar_arrive_expect_tx_relaxed(fb, bytes);
             bulk_load(dst, src, bytes, fb, pol);
         } else {
-            mbar_arrive(fb);
+            mbar_arrive_relaxed(fb);
         }
-        // the slot's record, then its tag
-        meta[lane] = make_int4(c.valid && sane ? c.s : -1, c.slot | (c.ks << 16), c.chunk, 0);
-        tag_store(tb, round * kRing + (uint32_t)lane);
+        tag_store(tb, round * kRing + (uint32_t)lane, (c.valid && sane) ? (uint32_t)it : 0xffffffffu);
         ++round;
-        it = claim_item(claim, lane, kRing, p.items);
+        it = it_next;
+        it_next = it < 0 ? -1 : claim_item(claim, lane, kRing, p.items);
         t_last = global_ns();
     }
     __syncwarp();
@@ -212,9 +244,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     Exp2Table* sT = reinterpret_cast<Exp2Table*>(smem + kSmemRing + kSmemTab);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSmemRing + kSmemTab + sizeof(Exp2Table));
     uint64_t* empty = full + kRing;
-    int4* meta = reinterpret_cast<int4*>(empty + kRing);
-    uint32_t* tag = reinterpret_cast<uint32_t*>(meta + kRing);
-    unsigned* next = tag + kRing;
+    unsigned long long* tag = reinterpret_cast<unsigned long long*>(empty + kRing);
+    unsigned* next = reinterpret_cast<unsigned*>(tag + kRing);
     unsigned* n_done = next + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -222,7 +253,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         for (int i = 0; i < kRing; ++i) {
             mbar_init(smem_u32(&full[i]), 1);
             mbar_init(smem_u32(&empty[i]), 1);
-            tag[i] = kTagNone;
+            tag[i] = (unsigned long long)kTagNone << 32;
         }
         *next = 0;
         *n_done = 0;
@@ -231,7 +262,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     __syncthreads();
     if (threadIdx.x == 0) griddep_launch_dependents();
     if (warp == 0) {
-        tma_producer<DT>(p, ring, full, empty, tag, meta, n_done, lane);
+        tma_producer<DT>(p, ring, full, empty, tag, n_done, lane);
         return;
     }
 
@@ -253,12 +284,13 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         if (lane == 0) k = atomicAdd(next, 1u);
         k = __shfl_sync(0xffffffffu, k, 0);
         const int slot = (int)(k % kRing);
-        uint32_t seen;
+        unsigned long long seen;
         if (!__all_sync(0xffffffffu, tag_wait(smem_u32(&tag[slot]), k, seen))) {
             if (lane == 0) raise_error(p.ws, kErrTimeout);
             break;
         }
-        if (__shfl_sync(0xffffffffu, seen, 0) == kTagDone) {
+        seen = __shfl_sync(0xffffffffu, seen, 0);
+        if ((uint32_t)(seen >> 32) == kTagDone) {
             // this slot has no more chunks; stop once no slot has any
             unsigned nd = 0;
             if (lane == 0) nd = *reinterpret_cast<volatile unsigned*>(n_done);
@@ -269,9 +301,12 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             if (lane == 0) raise_error(p.ws, kErrTimeout);
             break;
         }
-        const int4 md = ld_meta(smem_u32(&meta[slot]));
-        const int s = md.x, rs = md.y & 0xffff, ks = md.y >> 16, chunk = md.z;
-        const bool is_draft = rs < 2 * ks && (rs & 1);
+        const uint32_t item = (uint32_t)seen;  // 0xffffffff: a chunk with nothing to load
+        ChunkRef c{};
+        c.valid = false;
+        if (item != 0xffffffffu) c = chunk_ref(p, item);
+        const int s = c.valid ? c.s : -1, rs = c.slot, ks = c.ks, chunk = c.chunk;
+        const bool is_draft = c.is_draft;
         const unsigned char* cbuf = ring + (size_t)slot * kChunkBytes;
         const bool sane = s < 0 || (check_ok(p.ws, chunk >= 0 && chunk < p.cpr, -111, chunk) &&
                                     check_ok(p.ws, rs >= 0 && rs < p.slots, -112, rs));
@@ -281,6 +316,12 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 #pragma unroll
                 for (int v = 0; v < kLoads; ++v)
                     raw[v] = *reinterpret_cast<const uint4*>(cbuf + v * 512 + lane * 16);
+                // the chunk now sits in registers: hand the slot back before the arithmetic, so
+                // that the producer can refill it while this warp computes (the arrival follows
+                // an instruction that consumed every loaded word, so the reads are complete)
+                consume_all(raw);
+                __syncwarp();
+                if (lane == 0) mbar_arrive_relaxed(smem_u32(&empty[slot]));
                 if (chunk == p.cpr - 1) {  // the row's last chunk: mask past V
                     const long long base = (long long)chunk * Geo<DT>::kChunk + lane * Geo<DT>::kPerVec;
 #pragma unroll
@@ -299,10 +340,13 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                 float4* tot = ws_ptr<float4>(p.ws, p.L.ddtot) + (size_t)(s * 2) * p.cpr + chunk;
                 float4* sub = ws_ptr<float4>(p.ws, p.L.ddsub) + ((size_t)(s * 2) * p.cpr + chunk) * kSubs;
                 precise_core<DT>(src, e0 + SUB <= p.R.V, e0, p.R.V, lane, P, tot, sub);
+                __syncwarp();
+                if (lane == 0) mbar_arrive_relaxed(smem_u32(&empty[slot]));
             }
+        } else {
+            __syncwarp();
+            if (lane == 0) mbar_arrive_relaxed(smem_u32(&empty[slot]));
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
     }
 }
 
