@@ -10,9 +10,11 @@
 // the whole ring stays in flight; a precise chunk, read twice, keeps its slot until done. Every
 // logit crosses HBM exactly once.
 //
-// Chunks (sequence-major order) are dealt dynamically: producer lane j of every block claims the
-// next chunk of stripe j (chunks j, j+32, j+64, ...) from a grid-wide counter, so the blocks stay
-// balanced whatever the mix of fast and precise chunks they draw.
+// Chunks (sequence-major order) are dealt round-robin: block b loads chunks b, b+B, b+2B, ...
+// (B blocks), its producer lane j the ones numbered 32 * round + j among them. Every block draws
+// the same mix of fast and precise chunks (the precise rows recur every sequence), so the blocks
+// stay balanced without a shared counter; a claim from one would put an atomic round trip on
+// the producer's path.
 //
 // Every wait is bounded (about 2 s of wall time): a wait that runs out records
 // SMCSD_ERR_TIMEOUT in the workspace and the warp leaves; the producer, before it leaves,
@@ -31,7 +33,7 @@ constexpr size_t kSmemTab = (size_t)kTabAlloc * sizeof(float2);
 constexpr size_t kSmemBytes =
     kSmemRing + kSmemTab + sizeof(Exp2Table) + 2 * kRing * 8 + kRing * 8 + 16;
 constexpr uint32_t kTagNone = 0xffffffffu;  // slot never loaded
-constexpr uint32_t kTagDone = 0xfffffffeu;  // the slot's claimer has no more chunks
+constexpr uint32_t kTagDone = 0xfffffffeu;  // the slot's producer lane has no more chunks
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -47,7 +49,7 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 // Relaxed arrivals: they order nothing, so they never wait for this warp's outstanding global
-// accesses (claims, partial stores). Used where nothing written before the arrival is read by
+// accesses (partial stores). Used where nothing written before the arrival is read by
 // the waiting side (the data comes through the bulk copy or has already been read out).
 __device__ __forceinline__ void mbar_arrive_expect_tx_relaxed(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.relaxed.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
@@ -157,30 +159,25 @@ struct SmemBlock {
     }
 };
 
-// The producer warp: lane j owns slot j. It claims chunks from stripe j of the grid-wide
-// dealing (claim_item) and loads each into its slot once the consumer of the slot's previous
-// chunk has handed the slot back, then writes the slot's record (sequence, row slot and draft
-// count, chunk) and tags the slot with the block-local sequence number k = 32 * round + j. A lane whose stripe is used up tags its
-// slot kTagDone. The lanes poll their slots together (one non-blocking test per lane per pass),
-// so no lane spins alone while the others wait on it; the test does not block. Each lane keeps
-// its next two chunks claimed, so a claim's latency is hidden behind a whole refill.
+// The producer warp: lane j owns slot j and loads the block's chunks 32 * round + j into it,
+// each once the consumer of the slot's previous chunk has handed the slot back, then tags the
+// slot with the block-local sequence number k = 32 * round + j and the chunk's index. A lane out
+// of chunks tags its slot kTagDone. The lanes poll their slots together (one non-blocking test per
+// lane per pass), so no lane spins alone while the others wait on it.
 template <int DT>
 __device__ __noinline__ void tma_producer(const StreamParams& p, unsigned char* ring,
                                           uint64_t* full, uint64_t* empty,
                                           unsigned long long* tag, unsigned* n_done, int lane) {
-    unsigned* claim = ws_ptr<unsigned>(p.ws, p.L.claim);
     const long long row_bytes = (long long)p.R.V * Geo<DT>::kBytes;
     const uint32_t fb = smem_u32(&full[lane]), eb = smem_u32(&empty[lane]);
     const uint32_t tb = smem_u32(&tag[lane]);
     const uint32_t dst = smem_u32(ring + (size_t)lane * kChunkBytes);
     const uint64_t pol = l2_evict_first();
-    // two claims ahead: `it` is the lane's next chunk, `it_next` the one after, whose claim is in
-    // flight while `it` waits for the slot
-    long long it = claim_item(claim, lane, kRing, p.items);
-    long long it_next = claim_item(claim, lane, kRing, p.items);
     uint32_t round = 0;
     bool done = false;
-    unsigned long long t_last = global_ns();
+    unsigned streak = 0;  // failed polls in a row, and when the streak began
+    unsigned long long t_streak = 0;
+    const long long B = gridDim.x;
     bool moved = true;
     while (__any_sync(0xffffffffu, !done)) {
         // a pass in which no lane could refill its slot backs off briefly instead of spinning on
@@ -188,13 +185,19 @@ __device__ __noinline__ void tma_producer(const StreamParams& p, unsigned char* 
         if (!__any_sync(0xffffffffu, moved)) __nanosleep(200);
         moved = false;
         if (done) continue;
+        long long it;
         if (round > 0 && !mbar_test_wait(eb, (round - 1) & 1u)) {
-            if (global_ns() - t_last > kWaitLimitNs) {
-                raise_error(p.ws, kErrTimeout);
-                it = -1;  // give the slot up below so that its consumers stop
-            } else {
+            if (streak++ == 0) {
+                t_streak = global_ns();
                 continue;
             }
+            if ((streak & 1023u) != 0 || global_ns() - t_streak <= kWaitLimitNs) continue;
+            raise_error(p.ws, kErrTimeout);
+            it = -1;  // give the slot up below so that its consumers stop
+        } else {
+            streak = 0;
+            it = (long long)blockIdx.x + ((long long)round * kRing + lane) * B;
+            if (it >= p.items) it = -1;
         }
         moved = true;
         if (it < 0) {
@@ -224,12 +227,7 @@ __device__ __noinline__ void tma_producer(const StreamParams& p, unsigned char* 
         }
         tag_store(tb, round * kRing + (uint32_t)lane, (c.valid && sane) ? (uint32_t)it : 0xffffffffu);
         ++round;
-        it = it_next;
-        it_next = it < 0 ? -1 : claim_item(claim, lane, kRing, p.items);
-        t_last = global_ns();
     }
-    __syncwarp();
-    if (lane == 0) reset_claims(claim, kRing);
     // the copy of this lane's last chunk may still be in flight: wait for it before leaving
     if (round > 0) mbar_wait(fb, (round - 1) & 1u);
 }
