@@ -59,7 +59,7 @@ def algorithmic_bytes(cfg) -> int:
     return logit_bytes(cfg) + small
 
 
-KERNELS_PER_STEP = 3  # stream pass, finishing pass, group pass (the refcount memset is a copy-engine op)
+KERNELS_PER_STEP = 2  # stream pass and finishing pass (the refcount memset is a copy-engine op)
 
 
 def _source_sha256() -> str:
@@ -439,8 +439,8 @@ def run_gpu(args):
         "config": config,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "one smc_step call: stream_tma_kernel (82% of its device time), "
-                               "finish_kernel, group_kernel and the 64 KB refcount memset; "
+                     "kernel": "one smc_step call: stream_tma_kernel, finish_kernel and the 64 KB "
+                               "refcount memset (kernel shares in profiles/launches_<workload>.md); "
                                "achieved = algorithmic bytes per step / device time per step",
                      "traffic_source": "profiles/traffic_<workload>.txt (ncu dram bytes of one step)",
                      "peak_kind": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",

@@ -1,16 +1,15 @@
-// finish.cu -- the finishing passes after the streaming pass (smcsd_epilogue.cuh):
-//   finish_kernel  one block per sequence, one warp per row: the row's normaliser from its
-//                  chunk partials, or, for the bonus row of a particle, the drawn (K+1)-th
-//                  token; then warp 0 runs the sequence epilogue (SD ratio tests and hand-off, or
-//                  the SMC log-weight update);
-//   group_kernel   (fused step) one block per group: warp 0 computes the ESS and resamples, then
-//                  all warps remap the group's page-table rows.
+// finish.cu -- the finishing pass after the streaming pass (smcsd_epilogue.cuh), one block per
+// sequence, one warp per row: the row's normaliser from its chunk partials, or, for the bonus
+// row of a particle, the drawn (K+1)-th token; then warp 0 runs the sequence epilogue (SD ratio
+// tests and hand-off, or the SMC log-weight update). In the fused step the block of each group's
+// last particle (a counter per group, release on arrival, acquire by the last) then computes the
+// group's ESS and resampling on warp 0 and remaps its page-table rows with all threads.
 //
-// Running these after the stream instead of inside it keeps the stream free of per-chunk
+// Running this after the stream instead of inside it keeps the stream free of per-chunk
 // completion counts (each a device-scope release), and a block's barrier orders its rows before
-// its sequence epilogue, so no counter or fence is needed here either. Each pass is launched as a
-// programmatic dependent of the one before, so that its launch overlaps that pass's tail; it
-// waits for the earlier pass to complete before it reads anything the earlier pass wrote.
+// its sequence epilogue. The pass is launched as a programmatic dependent of the stream, so that
+// its launch overlaps the stream's tail; it waits for the stream to complete before it reads
+// anything the stream wrote.
 //
 // The bonus row's rescan evaluates the 64 weights of one lane block without the shared-memory
 // exp table: the general path gives the same weights as the table (the table holds exactly its
@@ -20,38 +19,12 @@
 namespace smcsd {
 
 constexpr int kFinishMaxWarps = 32;
-constexpr int kGroupThreads = 256;
 
-template <int DT, int MODE>
-__global__ void __launch_bounds__(kFinishMaxWarps * kWarp)
-    finish_kernel(const __grid_constant__ StreamParams p) {
-    __shared__ Exp2Table sT;
-    for (int i = threadIdx.x; i < 32; i += blockDim.x) {
-        sT.hi[i] = p.T.hi[i];
-        sT.lo[i] = p.T.lo[i];
-    }
-    __syncthreads();
-    griddep_wait();
-    if (threadIdx.x == 0) griddep_launch_dependents();
-    const PreciseCtx P{p.sc_t, &sT, nullptr, p.ws, p.direct};
-    const int s = blockIdx.x;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    const int ks = seq_len(p.R, s, p.ws);
-    if (ks < 0) return;  // (the same on every thread of the block)
-    for (int slot = warp; slot <= 2 * ks; slot += nw) row_epilogue<DT, MODE>(p, P, s, slot, ks, lane);
-    __syncthreads();
-    if (warp != 0) return;
-    if (MODE == kModeSD)
-        sd_seq_epilogue(p, s, ks, lane);
-    else
-        smc_particle_epilogue(p, s, lane);
-}
-
-__global__ void __launch_bounds__(kGroupThreads) group_kernel(const __grid_constant__ StreamParams p) {
-    extern __shared__ int32_t sAnc[];  // [N]
-    __shared__ int sRes;
-    griddep_wait();
-    const int g = blockIdx.x, N = p.N;
+// The fused step's group part, run by the block of the group's last particle: warp 0 computes the
+// ESS and resamples into shared memory, then all threads remap the group's page-table rows.
+__device__ __forceinline__ void group_part(const StreamParams& p, int g, int32_t* sAnc, int* sRes,
+                                           int bar, int nthr) {
+    const int N = p.N;
     const int lane = threadIdx.x & 31;
     int32_t* anc = p.ancestors + (size_t)g * N;
     if (threadIdx.x < kWarp) {
@@ -72,18 +45,59 @@ __global__ void __launch_bounds__(kGroupThreads) group_kernel(const __grid_const
             __syncwarp();
             for (int j = lane; j < N; j += kWarp) sAnc[j] = __ldcg(anc + j);
         }
-        if (lane == 0) sRes = res ? 1 : 0;
+        if (lane == 0) *sRes = res ? 1 : 0;
     }
-    __syncthreads();
+    bar_sync(bar, nthr);
     if (!p.table_in) return;
     const int P = p.pages_per_seq;
     const int32_t* tin = p.table_in + (size_t)g * N * P;
     int32_t* tout = p.table_out + (size_t)g * N * P;
-    const bool res = sRes != 0;
+    const bool res = *sRes != 0;
     if ((P & 3) == 0 && ((reinterpret_cast<uintptr_t>(tin) | reinterpret_cast<uintptr_t>(tout)) & 15u) == 0)
-        remap_rows_block<4>(p, tin, tout, sAnc, res, N, P);
+        remap_rows_block<4>(p, tin, tout, sAnc, res, N, P, nthr);
     else
-        remap_rows_block<1>(p, tin, tout, sAnc, res, N, P);
+        remap_rows_block<1>(p, tin, tout, sAnc, res, N, P, nthr);
+}
+
+template <int DT, int MODE>
+__global__ void __launch_bounds__(kFinishMaxWarps * kWarp)
+    finish_kernel(const __grid_constant__ StreamParams p) {
+    extern __shared__ int32_t sAnc[];  // [N] (fused step)
+    __shared__ Exp2Table sT;
+    __shared__ int sLast, sRes;
+    for (int i = threadIdx.x; i < 32; i += blockDim.x) {
+        sT.hi[i] = p.T.hi[i];
+        sT.lo[i] = p.T.lo[i];
+    }
+    __syncthreads();
+    griddep_wait();
+    const PreciseCtx P{p.sc_t, &sT, nullptr, p.ws, p.direct};
+    const int s = blockIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int ks = seq_len(p.R, s, p.ws);
+    if (ks < 0) return;  // (the same on every thread of the block)
+    for (int slot = warp; slot <= 2 * ks; slot += nw) row_epilogue<DT, MODE>(p, P, s, slot, ks, lane);
+    // The sequence (and group) epilogue needs only the rows with a draft token. When the block has
+    // a warp per row, the bonus row's warp (warp 2ks) keeps drawing while the others go on, meeting
+    // at a named barrier without it; otherwise the whole block meets.
+    const bool split = MODE != kModeSD && nw == 2 * ks + 1 && ks > 0;
+    if (split && warp == 2 * ks) return;
+    const int bar = split ? 1 : 0, nthr = split ? 2 * ks * kWarp : (int)blockDim.x;
+    bar_sync(bar, nthr);
+    if (warp == 0) {
+        if (MODE == kModeSD) {
+            sd_seq_epilogue(p, s, ks, lane);
+        } else {
+            smc_particle_epilogue(p, s, lane);
+            if (MODE == kModeSMCStep) {
+                const bool last = arrive_last(ws_ptr<unsigned>(p.ws, p.L.cnt_group) + s / p.N, (unsigned)p.N, lane);
+                if (lane == 0) sLast = last ? 1 : 0;
+            }
+        }
+    }
+    if (MODE != kModeSMCStep) return;
+    bar_sync(bar, nthr);
+    if (sLast) group_part(p, s / p.N, sAnc, &sRes, bar, nthr);
 }
 
 static cudaError_t launch_dependent(const void* kern, dim3 grid, dim3 block, size_t smem,
@@ -105,16 +119,14 @@ static cudaError_t launch_dependent(const void* kern, dim3 grid, dim3 block, siz
 template <int DT, int MODE>
 static cudaError_t launch_finish_t(const StreamParams& p, cudaStream_t st) {
     const int nw = p.slots < kFinishMaxWarps ? p.slots : kFinishMaxWarps;
-    cudaError_t e = launch_dependent(reinterpret_cast<const void*>(finish_kernel<DT, MODE>),
-                                     dim3((unsigned)p.R.S), dim3((unsigned)(nw * kWarp)), 0, p, st);
-    if (e != cudaSuccess || MODE != kModeSMCStep) return e;
-    const size_t smem = (size_t)p.N * sizeof(int32_t);
+    const size_t smem = MODE == kModeSMCStep ? (size_t)p.N * sizeof(int32_t) : 0;
+    auto kern = finish_kernel<DT, MODE>;
     if (smem > 48 * 1024) {
-        e = cudaFuncSetAttribute(group_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    return launch_dependent(reinterpret_cast<const void*>(group_kernel), dim3((unsigned)p.G),
-                            dim3(kGroupThreads), smem, p, st);
+    return launch_dependent(reinterpret_cast<const void*>(kern), dim3((unsigned)p.R.S),
+                            dim3((unsigned)(nw * kWarp)), smem, p, st);
 }
 
 cudaError_t launch_finish(const StreamParams& p, cudaStream_t st) {

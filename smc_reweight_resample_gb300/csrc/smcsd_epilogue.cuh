@@ -143,16 +143,16 @@ static __device__ __noinline__ void smc_particle_epilogue(const StreamParams& p,
     }
 }
 
-// Page-table rows of one group after resampling, by all threads of a block: row j of the output
+// Page-table rows of one group after resampling, by threads 0..nthr-1 of a block: row j of the output
 // is row anc[j] of the input (row j when the group was not resampled), W ints per access; every
 // non-empty page id is counted in refcount.
 template <int W>
 __device__ __forceinline__ void remap_rows_block(const StreamParams& p, const int32_t* tin, int32_t* tout,
-                                                 const int32_t* anc, bool res, int N, int P) {
+                                                 const int32_t* anc, bool res, int N, int P, int nthr) {
     using Vec = typename std::conditional<W == 4, int4, int>::type;
     const unsigned PW = (unsigned)(P / W);
     const unsigned n = (unsigned)N * PW;
-    for (unsigned e = threadIdx.x; e < n; e += blockDim.x) {
+    for (unsigned e = threadIdx.x; e < n; e += (unsigned)nthr) {
         const unsigned j = e / PW, col = e - j * PW;
         const int a = res ? anc[j] : (int)j;
         const Vec v = __ldg(reinterpret_cast<const Vec*>(tin + (size_t)a * P) + col);
