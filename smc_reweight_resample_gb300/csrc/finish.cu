@@ -62,21 +62,36 @@ __device__ __forceinline__ void group_part(const StreamParams& p, int g, int32_t
 template <int DT, int MODE>
 __global__ void __launch_bounds__(kFinishMaxWarps * kWarp)
     finish_kernel(const __grid_constant__ StreamParams p) {
-    extern __shared__ int32_t sAnc[];  // [N] (fused step)
+    // dynamic shared memory: row normalisers, draft tokens and the logits there per row slot,
+    // then (fused step) the group's ancestors
+    extern __shared__ __align__(16) unsigned char dsm[];
+    float2* sL = reinterpret_cast<float2*>(dsm);
+    int* sX = reinterpret_cast<int*>(sL + p.slots);
+    float* sZ = reinterpret_cast<float*>(sX + p.slots);
+    int32_t* sAnc = reinterpret_cast<int32_t*>(sZ + p.slots);
     __shared__ Exp2Table sT;
     __shared__ int sLast, sRes;
     for (int i = threadIdx.x; i < 32; i += blockDim.x) {
         sT.hi[i] = p.T.hi[i];
         sT.lo[i] = p.T.lo[i];
     }
-    __syncthreads();
-    griddep_wait();
-    const PreciseCtx P{p.sc_t, &sT, nullptr, p.ws, p.direct};
     const int s = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     const int ks = seq_len(p.R, s, p.ws);
+    // what does not depend on the streaming pass is read while it finishes
+    float lw_old = 0.0f;
+    if (ks >= 0) {
+        for (int slot = warp; slot < 2 * ks; slot += nw)
+            if (lane == 0) prefetch_token_logit<DT>(p, s, slot, sX, sZ);
+        if (MODE != kModeSD && threadIdx.x == 0) lw_old = __ldcg(p.logw + s);
+        if (MODE == kModeSMCStep && p.table_in && (int)threadIdx.x * 32 < p.pages_per_seq)
+            l2_prefetch(p.table_in + (size_t)s * p.pages_per_seq + threadIdx.x * 32);
+    }
+    __syncthreads();
+    griddep_wait();
     if (ks < 0) return;  // (the same on every thread of the block)
-    for (int slot = warp; slot <= 2 * ks; slot += nw) row_epilogue<DT, MODE>(p, P, s, slot, ks, lane);
+    const PreciseCtx P{p.sc_t, &sT, nullptr, p.ws, p.direct};
+    for (int slot = warp; slot <= 2 * ks; slot += nw) row_epilogue<DT, MODE>(p, P, s, slot, ks, lane, sL);
     // The sequence (and group) epilogue needs only the rows with a draft token. When the block has
     // a warp per row, the bonus row's warp (warp 2ks) keeps drawing while the others go on, meeting
     // at a named barrier without it; otherwise the whole block meets.
@@ -86,9 +101,9 @@ __global__ void __launch_bounds__(kFinishMaxWarps * kWarp)
     bar_sync(bar, nthr);
     if (warp == 0) {
         if (MODE == kModeSD) {
-            sd_seq_epilogue(p, s, ks, lane);
+            sd_seq_epilogue(p, s, ks, lane, sL, sX, sZ);
         } else {
-            smc_particle_epilogue(p, s, lane);
+            smc_particle_epilogue(p, s, lane, __shfl_sync(0xffffffffu, lw_old, 0), sL, sX, sZ);
             if (MODE == kModeSMCStep) {
                 const bool last = arrive_last(ws_ptr<unsigned>(p.ws, p.L.cnt_group) + s / p.N, (unsigned)p.N, lane);
                 if (lane == 0) sLast = last ? 1 : 0;
@@ -119,7 +134,8 @@ static cudaError_t launch_dependent(const void* kern, dim3 grid, dim3 block, siz
 template <int DT, int MODE>
 static cudaError_t launch_finish_t(const StreamParams& p, cudaStream_t st) {
     const int nw = p.slots < kFinishMaxWarps ? p.slots : kFinishMaxWarps;
-    const size_t smem = MODE == kModeSMCStep ? (size_t)p.N * sizeof(int32_t) : 0;
+    const size_t smem = (size_t)p.slots * (sizeof(float2) + sizeof(int) + sizeof(float)) +
+                        (MODE == kModeSMCStep ? (size_t)p.N * sizeof(int32_t) : 0);
     auto kern = finish_kernel<DT, MODE>;
     if (smem > 48 * 1024) {
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -26,11 +26,11 @@ __device__ __forceinline__ void load_exp2_table(const Exp2Table& src, Exp2Table&
     __syncthreads();
 }
 
-// One row: the row's normaliser and the logit at its draft token, or, for the bonus row of a
-// particle, the (K+1)-th token drawn from pi with the row's normaliser as a by-product.
+// One row: the row's normaliser (into sL[slot], and the optional lse outputs), or, for the bonus
+// row of a particle, the (K+1)-th token drawn from pi with the row's normaliser as a by-product.
 template <int DT, int MODE>
 __device__ __noinline__ void row_epilogue(const StreamParams& p, const PreciseCtx& P, int s, int slot,
-                                          int ks, int lane) {
+                                          int ks, int lane, float2* sL) {
     const Rows& R = p.R;
     const int k = slot >> 1;
     if (MODE != kModeSD && slot == 2 * ks) {
@@ -49,20 +49,11 @@ __device__ __noinline__ void row_epilogue(const StreamParams& p, const PreciseCt
     }
     const bool is_draft = slot < 2 * ks && (slot & 1);
     const size_t r = (size_t)s * p.slots + slot;
-    // the logit at the row's draft token (its load overlaps the normaliser's)
-    float zx = 0.0f;
-    if (lane == 0 && slot < 2 * ks) {
-        const int x = __ldg(R.toks + drow_of(R, s, k));
-        if (x >= 0 && x < R.V)
-            zx = is_draft ? logit_at<DT>(row_ptr<DT>(R.drf, drow_of(R, s, k), R.V), x)
-                          : logit_at<DT>(row_ptr<DT>(R.tgt, trow_of(R, s, k), R.V), x);
-    }
     const dd L = row_lse_fast(ws_ptr<float2>(p.ws, p.L.fast) + r * p.cpr, p.cpr,
                               is_draft ? p.sc_d : p.sc_t, lane);
     if (lane == 0) {
-        if (slot < 2 * ks) ws_ptr<float>(p.ws, p.L.zsel)[r] = zx;
         if (!(L.hi == L.hi)) raise_error(p.ws, kErrNonfinite);  // a row without mass
-        ws_ptr<float2>(p.ws, p.L.rowL)[r] = make_float2(L.hi, L.lo);
+        sL[slot] = make_float2(L.hi, L.lo);
         const float Lf = f_add(L.hi, L.lo);
         if (is_draft) {
             if (p.lse_drf) p.lse_drf[drow_of(R, s, k)] = Lf;
@@ -72,24 +63,37 @@ __device__ __noinline__ void row_epilogue(const StreamParams& p, const PreciseCt
     }
 }
 
-// log p_k(x_k) - log q_k(x_k) at position k of sequence s, as a double-float, from the row
-// normalisers and the logits recorded at the draft token. False (with an error raised) if the
-// token is out of range.
-__device__ __forceinline__ bool log_ratio(const StreamParams& p, int s, int k, dd& ell) {
+// Inputs of the sequence epilogue that do not depend on the streaming pass, read before waiting
+// for it: the draft token of row `slot` (< 2ks) and the logit there, into sX[slot], sZ[slot].
+template <int DT>
+__device__ __forceinline__ void prefetch_token_logit(const StreamParams& p, int s, int slot, int* sX,
+                                                     float* sZ) {
     const Rows& R = p.R;
+    const int k = slot >> 1;
+    const bool is_draft = slot & 1;
     const int x = __ldg(R.toks + drow_of(R, s, k));
-    const size_t r = (size_t)s * p.slots + 2 * k;
-    const float2* rowL = ws_ptr<float2>(p.ws, p.L.rowL);
-    const float* zsel = ws_ptr<float>(p.ws, p.L.zsel);
-    const float2 Lt = __ldcg(rowL + r), Ld = __ldcg(rowL + r + 1);
-    const float zt = __ldcg(zsel + r), zd = __ldcg(zsel + r + 1);
+    float z = 0.0f;
+    if (x >= 0 && x < R.V)
+        z = is_draft ? logit_at<DT>(row_ptr<DT>(R.drf, drow_of(R, s, k), R.V), x)
+                     : logit_at<DT>(row_ptr<DT>(R.tgt, trow_of(R, s, k), R.V), x);
+    sX[slot] = x;
+    sZ[slot] = z;
+}
+
+// log p_k(x_k) - log q_k(x_k) at position k, as a double-float, from the row normalisers sL and
+// the draft token and logits there (sX, sZ) of this sequence's block. False (with an error raised)
+// if the token is out of range.
+__device__ __forceinline__ bool log_ratio(const StreamParams& p, int k, const float2* sL, const int* sX,
+                                          const float* sZ, dd& ell) {
+    const int x = sX[2 * k];
     ell = dd{0.0f, 0.0f};
-    if (x < 0 || x >= R.V) {
+    if (x < 0 || x >= p.R.V) {
         raise_error(p.ws, kErrRange);
         return false;
     }
-    const dd lt = dd_sub(dd_mul_f(dd{p.sc_t.c_hi, p.sc_t.c_lo}, zt), dd{Lt.x, Lt.y});
-    const dd ld = dd_sub(dd_mul_f(dd{p.sc_d.c_hi, p.sc_d.c_lo}, zd), dd{Ld.x, Ld.y});
+    const float2 Lt = sL[2 * k], Ld = sL[2 * k + 1];
+    const dd lt = dd_sub(dd_mul_f(dd{p.sc_t.c_hi, p.sc_t.c_lo}, sZ[2 * k]), dd{Lt.x, Lt.y});
+    const dd ld = dd_sub(dd_mul_f(dd{p.sc_d.c_hi, p.sc_d.c_lo}, sZ[2 * k + 1]), dd{Ld.x, Ld.y});
     ell = dd_sub(lt, ld);
     return true;
 }
@@ -97,7 +101,8 @@ __device__ __forceinline__ bool log_ratio(const StreamParams& p, int s, int k, d
 // SD: the ratio tests min(1, p/q) in position order, the acceptance length and the hand-off of
 // the row (pair) to draw the final token from. Position k is accepted iff u_k < exp(min(0, l_k)),
 // with the exponential in double-float.
-static __device__ __noinline__ void sd_seq_epilogue(const StreamParams& p, int s, int ks, int lane) {
+static __device__ __noinline__ void sd_seq_epilogue(const StreamParams& p, int s, int ks, int lane,
+                                                    const float2* sL, const int* sX, const float* sZ) {
     const Rows& R = p.R;
     const float* u = p.uniforms + (size_t)s * (R.K + 1);
     int acc = ks;
@@ -106,7 +111,7 @@ static __device__ __noinline__ void sd_seq_epilogue(const StreamParams& p, int s
         bool rej = false;
         if (k < ks) {
             dd ell;
-            const bool ok = log_ratio(p, s, k, ell);
+            const bool ok = log_ratio(p, k, sL, sX, sZ, ell);
             const float uk = __ldg(u + k);
             if (!ok || !(ell.hi == ell.hi)) {
                 rej = true;
@@ -129,16 +134,18 @@ static __device__ __noinline__ void sd_seq_epilogue(const StreamParams& p, int s
     }
 }
 
-// SMC: log-weight update sum_k log pi_k(x_k) - log q_k(x_k) of particle s (double-float sums).
-static __device__ __noinline__ void smc_particle_epilogue(const StreamParams& p, int s, int lane) {
+// SMC: log-weight update sum_k log pi_k(x_k) - log q_k(x_k) of particle s (double-float sums),
+// from its old log-weight lw_old.
+static __device__ __noinline__ void smc_particle_epilogue(const StreamParams& p, int s, int lane, float lw_old,
+                                                          const float2* sL, const int* sX, const float* sZ) {
     dd inc{0.0f, 0.0f};
     for (int k = lane; k < p.R.K; k += kWarp) {
         dd ell;
-        if (log_ratio(p, s, k, ell)) inc = dd_add(inc, ell);
+        if (log_ratio(p, k, sL, sX, sZ, ell)) inc = dd_add(inc, ell);
     }
     inc = warp_sum_dd(inc);
     if (lane == 0) {
-        const dd lw = dd_add(dd{__ldcg(p.logw + s), 0.0f}, inc);
+        const dd lw = dd_add(dd{lw_old, 0.0f}, inc);
         p.logw[s] = f_add(lw.hi, lw.lo);
     }
 }
