@@ -184,6 +184,31 @@ struct ChunkRef {
     bool valid, is_draft;
     long long row;
 };
+// Chunk of the two-list dealing: `tag_item` is an index into the precise list (high bit set: the
+// bonus row of a particle, cpr chunks per particle) or into the fast list (fslots rows of cpr
+// chunks per sequence, row slots 0..fslots-1).
+__device__ __forceinline__ ChunkRef chunk_ref_two_list(const StreamParams& p, uint32_t tag_item) {
+    ChunkRef c;
+    if (tag_item & 0x80000000u) {
+        const uint32_t i = tag_item & 0x7fffffffu;
+        c.s = (int)fast_div(i, p.div_cpr);
+        c.chunk = (int)(i - (uint32_t)c.s * p.div_cpr.d);
+        c.ks = seq_len(p.R, c.s, p.ws);
+        c.slot = 2 * c.ks;
+    } else {
+        c.s = (int)fast_div(tag_item, p.div_fseq);
+        const uint32_t rem = tag_item - (uint32_t)c.s * p.div_fseq.d;
+        c.slot = (int)fast_div(rem, p.div_cpr);
+        c.chunk = (int)(rem - (uint32_t)c.slot * p.div_cpr.d);
+        c.ks = seq_len(p.R, c.s, p.ws);
+    }
+    c.valid = c.ks >= 0 && c.slot <= 2 * c.ks;
+    c.is_draft = c.slot < 2 * c.ks && (c.slot & 1);
+    const int k = c.slot >> 1;
+    c.row = c.valid ? (c.is_draft ? drow_of(p.R, c.s, k) : trow_of(p.R, c.s, k)) : 0;
+    return c;
+}
+
 // Within a sequence the rows come bonus row first (position 0 is row slot 2ks, position q > 0 is
 // slot q - 1), so that the bonus row's draw, the longest row epilogue, overlaps the streaming of
 // the sequence's other rows instead of following its last chunk.

@@ -45,6 +45,11 @@ struct StreamParams {
     long long items;       // chunks in the sequence-major order (< 2^31)
     FastDiv div_seq;       // by slots * cpr (chunks per sequence)
     FastDiv div_cpr;       // by cpr (chunks per row)
+    // two-list dealing of the pipelined pass (set by its launcher): the precise chunks (rows that
+    // are sampled) and the fast chunks (all other rows, fslots per sequence) as separate lists
+    long long n_precise, n_fast;
+    int fslots;
+    FastDiv div_fseq;      // by fslots * cpr
 };
 
 // SD second and third passes (precise sums of the rows to draw from, the residual draw).

@@ -10,11 +10,12 @@
 // the whole ring stays in flight; a precise chunk, read twice, keeps its slot until done. Every
 // logit crosses HBM exactly once.
 //
-// Chunks (sequence-major order) are dealt round-robin: block b loads chunks b, b+B, b+2B, ...
-// (B blocks), its producer lane j the ones numbered 32 * round + j among them. Every block draws
-// the same mix of fast and precise chunks (the precise rows recur every sequence), so the blocks
-// stay balanced without a shared counter; a claim from one would put an atomic round trip on
-// the producer's path.
+// Chunks are dealt from two lists, each round-robin over the B blocks: the precise chunks (the
+// rows that are sampled, one per particle) and the fast chunks (all other rows). Block b takes
+// chunks b, b+B, b+2B, ... of each list and interleaves them, one precise chunk to fslots fast
+// ones, so every block gets the same share of each kind spread evenly over the pass, without a
+// shared counter (a claim from one would put an atomic round trip on the producer's path).
+// Producer lane j loads the block's local chunks 32 * round + j.
 //
 // Every wait is bounded (about 2 s of wall time): a wait that runs out records
 // SMCSD_ERR_TIMEOUT in the workspace and the warp leaves; the producer, before it leaves,
@@ -177,7 +178,32 @@ __device__ __noinline__ void tma_producer(const StreamParams& p, unsigned char* 
     bool done = false;
     unsigned streak = 0;  // failed polls in a row, and when the streak began
     unsigned long long t_streak = 0;
-    const long long B = gridDim.x;
+    // this block's shares of the two lists and how they interleave: groups of one precise chunk
+    // and fslots fast ones while both last (phase 1, local chunks k < L1), then the rest of the
+    // longer list. Each lane tracks its k = q * m + r (m = fslots + 1) incrementally, in 32-bit
+    // arithmetic (every index is below 2^31), so a refill costs no division.
+    const uint32_t Bu = gridDim.x, bu = blockIdx.x, m = (uint32_t)p.fslots + 1u;
+    const uint32_t Pb = p.n_precise > (long long)bu ? (uint32_t)((p.n_precise - 1 - bu) / Bu) + 1u : 0u;
+    const uint32_t Fb = p.n_fast > (long long)bu ? (uint32_t)((p.n_fast - 1 - bu) / Bu) + 1u : 0u;
+    const uint32_t G1 = p.fslots > 0 ? min(Pb, Fb / (uint32_t)p.fslots) : 0u;
+    const uint32_t L1 = G1 * m, Fr = Fb - G1 * (uint32_t)p.fslots;
+    const uint32_t dq = kRing / m, dr = kRing % m;  // k += 32 moves q by dq and r by dr
+    uint32_t k = (uint32_t)lane, q = k / m, r = k % m;
+    auto local_item = [&]() -> long long {  // tag item of local chunk k, or -1
+        uint32_t j;
+        bool precise;
+        if (k < L1) {
+            precise = r == 0;
+            j = precise ? q : q * (uint32_t)p.fslots + r - 1u;
+        } else {
+            const uint32_t k2 = k - L1;
+            precise = k2 >= Fr;
+            j = precise ? G1 + (k2 - Fr) : G1 * (uint32_t)p.fslots + k2;
+            if (precise && j >= Pb) return -1;
+        }
+        const uint32_t g = j * Bu + bu;
+        return precise ? (long long)(g | 0x80000000u) : (long long)g;
+    };
     bool moved = true;
     while (__any_sync(0xffffffffu, !done)) {
         // a pass in which no lane could refill its slot backs off briefly instead of spinning on
@@ -196,8 +222,7 @@ __device__ __noinline__ void tma_producer(const StreamParams& p, unsigned char* 
             it = -1;  // give the slot up below so that its consumers stop
         } else {
             streak = 0;
-            it = (long long)blockIdx.x + ((long long)round * kRing + lane) * B;
-            if (it >= p.items) it = -1;
+            it = local_item();
         }
         moved = true;
         if (it < 0) {
@@ -206,7 +231,7 @@ __device__ __noinline__ void tma_producer(const StreamParams& p, unsigned char* 
             done = true;
             continue;
         }
-        const ChunkRef c = chunk_ref(p, (uint32_t)it);
+        const ChunkRef c = chunk_ref_two_list(p, (uint32_t)it);
         const long long off = (long long)c.chunk * kChunkBytes;
         const long long left = row_bytes - off;
         const uint32_t bytes = (uint32_t)(left < kChunkBytes ? left : kChunkBytes);
@@ -227,6 +252,13 @@ __device__ __noinline__ void tma_producer(const StreamParams& p, unsigned char* 
         }
         tag_store(tb, round * kRing + (uint32_t)lane, (c.valid && sane) ? (uint32_t)it : 0xffffffffu);
         ++round;
+        k += kRing;
+        q += dq;
+        r += dr;
+        if (r >= m) {
+            r -= m;
+            ++q;
+        }
     }
     // the copy of this lane's last chunk may still be in flight: wait for it before leaving
     if (round > 0) mbar_wait(fb, (round - 1) & 1u);
@@ -302,7 +334,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         const uint32_t item = (uint32_t)seen;  // 0xffffffff: a chunk with nothing to load
         ChunkRef c{};
         c.valid = false;
-        if (item != 0xffffffffu) c = chunk_ref(p, item);
+        if (item != 0xffffffffu) c = chunk_ref_two_list(p, item);
         const int s = c.valid ? c.s : -1, rs = c.slot, ks = c.ks, chunk = c.chunk;
         const bool is_draft = c.is_draft;
         const unsigned char* cbuf = ring + (size_t)slot * kChunkBytes;
@@ -349,13 +381,20 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 }
 
 template <int DT, int MODE>
-static cudaError_t launch_tma_t(const StreamParams& p, cudaStream_t st) {
+static cudaError_t launch_tma_t(const StreamParams& p0, cudaStream_t st) {
     auto kern = stream_tma_kernel<DT, MODE>;
+    StreamParams p = p0;
+    // the sampled rows (one per particle) form the precise list; in SD mode every row is fast
+    const bool sampled = MODE != kModeSD;
+    p.fslots = sampled ? p.slots - 1 : p.slots;
+    p.n_precise = sampled ? (long long)p.R.S * p.cpr : 0;
+    p.n_fast = (long long)p.R.S * p.fslots * p.cpr;
+    p.div_fseq = make_fastdiv((uint32_t)(p.fslots > 0 ? p.fslots * p.cpr : 1));
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     const long long cap = device_sm_count();
-    const long long want = (p.items + kTmaConsumers - 1) / kTmaConsumers;
+    const long long want = (p.n_precise + p.n_fast + kTmaConsumers - 1) / kTmaConsumers;
     int grid = (int)(want < cap ? want : cap);
     if (grid < 1) grid = 1;
     kern<<<grid, kTmaThreads, kSmemBytes, st>>>(p);
