@@ -1,8 +1,9 @@
 // stream_tma.cu -- the streaming pass over 16-byte-aligned logits rows as a TMA pipeline.
 //
-// One block per SM: a producer warp that moves 4 KB chunks of logits from HBM into a ring of
+// One block per SM: two producer warps that move 4 KB chunks of logits from HBM into a ring of
 // kRing = 32 shared-memory slots with the bulk-copy engine (cp.async.bulk, completion counted on
-// one mbarrier per slot; lane j of the producer fills slot j), and kTmaConsumers consumer warps
+// one mbarrier per slot; lane j < 16 of producer warp w fills slot 16 w + j, so the two warps'
+// refills run side by side on two sub-partitions), and kTmaConsumers consumer warps
 // that take the slots in the order they were filled from a shared counter, wait for theirs and
 // compute the chunk's partial (fast or precise, smcsd_sampling.cuh) into the workspace, where
 // the finishing pass (finish.cu) picks the partials up. A fast chunk is copied into registers
@@ -15,7 +16,7 @@
 // chunks b, b+B, b+2B, ... of each list and interleaves them, one precise chunk to fslots fast
 // ones, so every block gets the same share of each kind spread evenly over the pass, without a
 // shared counter (a claim from one would put an atomic round trip on the producer's path).
-// Producer lane j loads the block's local chunks 32 * round + j.
+// The producer lane of slot j loads the block's local chunks 32 * round + j.
 //
 // Every wait is bounded (about 2 s of wall time): a wait that runs out records
 // SMCSD_ERR_TIMEOUT in the workspace and the warp leaves; the producer, before it leaves,
@@ -25,7 +26,8 @@
 namespace smcsd {
 
 constexpr int kTmaConsumers = 18;
-constexpr int kTmaThreads = (kTmaConsumers + 1) * kWarp;
+constexpr int kTmaProducers = 2;                      // producer warps, kRing / 2 slots each
+constexpr int kTmaThreads = (kTmaConsumers + kTmaProducers) * kWarp;
 constexpr int kRing = kWarp;  // one slot per producer lane
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
@@ -160,22 +162,23 @@ struct SmemBlock {
     }
 };
 
-// The producer warp: lane j owns slot j and loads the block's chunks 32 * round + j into it,
+// A producer lane: it owns slot `slot` and loads the block's chunks 32 * round + slot into it,
 // each once the consumer of the slot's previous chunk has handed the slot back, then tags the
-// slot with the block-local sequence number k = 32 * round + j and the chunk's index. A lane out
+// slot with the block-local sequence number k = 32 * round + slot and the chunk's index. A lane out
 // of chunks tags its slot kTagDone. The lanes poll their slots together (one non-blocking test per
 // lane per pass), so no lane spins alone while the others wait on it.
 template <int DT>
 __device__ __noinline__ void tma_producer(const StreamParams& p, unsigned char* ring,
                                           uint64_t* full, uint64_t* empty,
-                                          unsigned long long* tag, unsigned* n_done, int lane) {
+                                          unsigned long long* tag, unsigned* n_done, int slot,
+                                          bool active) {
     const long long row_bytes = (long long)p.R.V * Geo<DT>::kBytes;
-    const uint32_t fb = smem_u32(&full[lane]), eb = smem_u32(&empty[lane]);
-    const uint32_t tb = smem_u32(&tag[lane]);
-    const uint32_t dst = smem_u32(ring + (size_t)lane * kChunkBytes);
+    const uint32_t fb = smem_u32(&full[slot]), eb = smem_u32(&empty[slot]);
+    const uint32_t tb = smem_u32(&tag[slot]);
+    const uint32_t dst = smem_u32(ring + (size_t)slot * kChunkBytes);
     const uint64_t pol = l2_evict_first();
     uint32_t round = 0;
-    bool done = false;
+    bool done = !active;
     unsigned streak = 0;  // failed polls in a row, and when the streak began
     unsigned long long t_streak = 0;
     // this block's shares of the two lists and how they interleave: groups of one precise chunk
@@ -188,7 +191,7 @@ __device__ __noinline__ void tma_producer(const StreamParams& p, unsigned char* 
     const uint32_t G1 = p.fslots > 0 ? min(Pb, Fb / (uint32_t)p.fslots) : 0u;
     const uint32_t L1 = G1 * m, Fr = Fb - G1 * (uint32_t)p.fslots;
     const uint32_t dq = kRing / m, dr = kRing % m;  // k += 32 moves q by dq and r by dr
-    uint32_t k = (uint32_t)lane, q = k / m, r = k % m;
+    uint32_t k = (uint32_t)slot, q = k / m, r = k % m;
     auto local_item = [&]() -> long long {  // tag item of local chunk k, or -1
         uint32_t j;
         bool precise;
@@ -250,7 +253,7 @@ __device__ __noinline__ void tma_producer(const StreamParams& p, unsigned char* 
         } else {
             mbar_arrive_relaxed(fb);
         }
-        tag_store(tb, round * kRing + (uint32_t)lane, (c.valid && sane) ? (uint32_t)it : 0xffffffffu);
+        tag_store(tb, round * kRing + (uint32_t)slot, (c.valid && sane) ? (uint32_t)it : 0xffffffffu);
         ++round;
         k += kRing;
         q += dq;
@@ -291,13 +294,14 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     }
     __syncthreads();
     if (threadIdx.x == 0) griddep_launch_dependents();
-    if (warp == 0) {
-        tma_producer<DT>(p, ring, full, empty, tag, n_done, lane);
+    if (warp < kTmaProducers) {
+        constexpr int kPer = kRing / kTmaProducers;
+        tma_producer<DT>(p, ring, full, empty, tag, n_done, warp * kPer + (lane % kPer), lane < kPer);
         return;
     }
 
     // consumers: tables first (while the producer already streams), then chunks
-    const int tid = threadIdx.x - kWarp, nthr = kTmaConsumers * kWarp;
+    const int tid = threadIdx.x - kTmaProducers * kWarp, nthr = kTmaConsumers * kWarp;
     for (int i = tid; i < 32; i += nthr) {
         sT->hi[i] = p.T.hi[i];
         sT->lo[i] = p.T.lo[i];
