@@ -114,7 +114,7 @@ __device__ __noinline__ void sd_rows_epilogue(const SampleParams& p, const Preci
 template <int DT>
 __global__ void __launch_bounds__(kSampleThreads) sd_rows_kernel(const __grid_constant__ SampleParams p) {
     __shared__ Exp2Table sT;
-    __shared__ float2 sTab[DT == 1 ? kTabAlloc : 1];
+    extern __shared__ __align__(16) float2 sTab[];  // kTabSize entries when the table is used
     load_exp2_table_s(p.T, sT);
     PreciseCtx P{p.sc, &sT, nullptr, p.ws, p.direct};
     if (DT == 1 && p.use_table) {
@@ -175,7 +175,7 @@ template <int DT>
 __global__ void __launch_bounds__(kSampleThreads)
     sd_residual_kernel(const __grid_constant__ SampleParams p) {
     __shared__ Exp2Table sT;
-    __shared__ float2 sTab[DT == 1 ? kTabAlloc : 1];
+    extern __shared__ __align__(16) float2 sTab[];  // kTabSize entries when the table is used
     load_exp2_table_s(p.T, sT);
     PreciseCtx P{p.sc, &sT, nullptr, p.ws, p.direct};
     if (DT == 1 && p.use_table) {
@@ -223,9 +223,9 @@ __global__ void __launch_bounds__(kSampleThreads)
 }
 
 template <typename Kern>
-static int grid_for(Kern kern, long long warps_needed) {
+static int grid_for(Kern kern, long long warps_needed, size_t smem) {
     int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kSampleThreads, 0) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kSampleThreads, smem) != cudaSuccess)
         occ = 1;
     const int wpb = kSampleThreads / kWarp;
     const long long want = (warps_needed + wpb - 1) / wpb;
@@ -236,12 +236,16 @@ static int grid_for(Kern kern, long long warps_needed) {
 
 template <int DT>
 static cudaError_t launch_sd_sample_t(const SampleParams& p, cudaStream_t st) {
+    const size_t smem = (DT == 1 && p.use_table) ? (size_t)kTabSize * sizeof(float2) : 0;
     auto k2 = sd_rows_kernel<DT>;
-    k2<<<grid_for(k2, (long long)p.R.S * 2 * p.cpr), kSampleThreads, 0, st>>>(p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
     auto k3 = sd_residual_kernel<DT>;
-    k3<<<grid_for(k3, (long long)p.R.S * p.cpr), kSampleThreads, 0, st>>>(p);
+    cudaError_t e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k2<<<grid_for(k2, (long long)p.R.S * 2 * p.cpr, smem), kSampleThreads, smem, st>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    k3<<<grid_for(k3, (long long)p.R.S * p.cpr, smem), kSampleThreads, smem, st>>>(p);
     return cudaGetLastError();
 }
 

@@ -60,6 +60,15 @@ __host__ __device__ inline int chunks_per_row(int V, int dtype) {
     return (V + ch - 1) / ch;
 }
 
+// Geometry of the exp table of precise weights (bf16 logits): one entry per bf16 magnitude in
+// [2^-24, 64) for each sign, the positive ones at [0, kTabHalf), the negative ones at
+// [kTabStride, kTabStride + kTabHalf), each half followed by a zero entry.
+constexpr uint32_t kTabMagLo = 0x3380u;                 // bf16 bits of 2^-24
+constexpr uint32_t kTabMagHi = 0x4280u;                 // bf16 bits of 64
+constexpr uint32_t kTabHalf = kTabMagHi - kTabMagLo;    // 3840 magnitudes per sign
+constexpr uint32_t kTabStride = kTabHalf + 1u;          // offset of the negative half
+constexpr int kTabSize = 2 * (int)kTabStride;           // 7682 entries, the two zero entries included
+
 // ------------------------------------------------------------------------------------------
 // workspace layout
 // ------------------------------------------------------------------------------------------
@@ -90,7 +99,7 @@ struct WsLayout {
     size_t seq;        // SeqState [S]
     size_t rowL;       // float2 [S * (2K+1)] row normalisers log sum_i exp(c z_i), double-float
     size_t zsel;       // float  [S * (2K+1)]  logit of the row at its draft token
-    size_t tab;        // cached exp table: 4 tag words + 4608 float2 (see setup_exp_table)
+    size_t tab;        // cached exp table: 4 tag words + kTabSize float2 (see setup_exp_table)
     size_t total;
 };
 
@@ -133,7 +142,7 @@ inline WsLayout ws_layout(int S, int K, int V) {
     L.zsel = o;
     o = align256(o + 4 * s * (2 * k + 1));
     L.tab = o;
-    o = align256(o + 16 + 8 * 4608);
+    o = align256(o + 16 + 8 * (size_t)kTabSize);
     L.total = o;
     return L;
 }

@@ -33,15 +33,11 @@ struct Scale {
 // ------------------------------------------------------------------------------------------
 //
 // exp(c z) is represented as e * 2^n with n = floor(z * c2) computed in float and e (about
-// [1, 2)) a double-float. For bf16 logits with 2^-12 <= |z| < 64, e comes from a table over all
-// such bf16 values (4608 entries, filled per block from the general routine below, so both give
-// identical bits); other logits use the general routine (double-float exp_split).
+// [1, 2)) a double-float. For bf16 logits with 2^-24 <= |z| < 64, e comes from a table over all
+// such bf16 values (kTabSize entries with the zero entries, layout in smcsd_internal.cuh, filled
+// from the general routine below, so both give identical bits); other logits use the general
+// routine (double-float exp_split).
 
-constexpr uint32_t kTabMagLo = 0x3980u;        // bf16 bits of 2^-12
-constexpr uint32_t kTabMagHi = 0x4280u;        // bf16 bits of 64
-constexpr uint32_t kTabHalf = kTabMagHi - kTabMagLo;  // entries per sign
-constexpr int kTabSize = 2 * (int)kTabHalf;    // 4608
-constexpr int kTabAlloc = kTabSize + 2;         // entries a table takes: kTabSize and kTabSize+1 are zero
 // the table is used only while |64 * c2| stays far inside floor_int's range
 constexpr double kTabMaxScale = 4096.0;
 
@@ -54,9 +50,9 @@ struct PreciseCtx {
 };
 
 // With c * 64 * log2(e) <= 125 every table value exp(c z), |z| < 64, is a normal float, so the
-// table can hold the double-float value itself; then a logit's weight relative to 2^nref is one
-// table load and two multiplies. Chunks whose largest weight is below 2^-60 use the general
-// routine instead (their low words would be subnormal).
+// table can hold the double-float value itself; then a logit's weight is one table load, and a
+// block's sum is scaled by 2^-nref once. Chunks whose largest weight is below 2^-60 (their low
+// words would be subnormal) or above 2^119 use the general routine instead.
 constexpr double kDirectMaxScale = 1.35;
 constexpr int kDirectMinRef = -60;
 
@@ -98,8 +94,13 @@ __device__ __forceinline__ void bar_sync(int id, int nthreads) {
 __device__ __forceinline__ void build_exp_table(float2* tab, const Scale& sc, const Exp2Table* T,
                                                 void* ws, bool direct, int tid, int nthr, int bar) {
     for (int i = tid; i < kTabSize; i += nthr) {
-        const uint32_t mag = kTabMagLo + (uint32_t)(i % (int)kTabHalf);
-        const uint32_t b = mag | (i >= (int)kTabHalf ? 0x8000u : 0u);
+        const bool neg = i >= (int)kTabStride;
+        const uint32_t m = (uint32_t)i - (neg ? kTabStride : 0u);
+        if (m == kTabHalf) {  // the zero entry after each half
+            tab[i] = make_float2(0.0f, 0.0f);
+            continue;
+        }
+        const uint32_t b = (kTabMagLo + m) | (neg ? 0x8000u : 0u);
         const GW g = general_weight(__uint_as_float(b << 16), sc.c_hi, sc.c_lo, sc.c2, T, ws);
         if (direct) {
             const float t = pow2i(g.n);
@@ -121,8 +122,6 @@ __device__ __forceinline__ void setup_exp_table(float2* tab, const Scale& sc, co
                                                 int tid, int nthr, int bar) {
     __shared__ int state;  // 0: build and publish, 1: copy, 2: build only
     if (tid == 0) {
-        tab[kTabSize] = make_float2(0.0f, 0.0f);  // the zero entries (never published or copied)
-        tab[kTabSize + 1] = make_float2(0.0f, 0.0f);
         uint32_t magic;
         asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(magic) : "l"(gtag) : "memory");
         if (magic != kTabMagic)
@@ -168,7 +167,7 @@ __device__ __forceinline__ dd precise_weight(uint32_t b, int nref, const Precise
     if (DT == 1 && P.tab && (!P.direct || nref >= kDirectMinRef)) {
         const uint32_t off = (b & 0x7fffu) - kTabMagLo;
         if (off < kTabHalf) {
-            const float2 e = P.tab[off + ((b & 0x8000u) ? kTabHalf : 0u)];
+            const float2 e = P.tab[off + ((b & 0x8000u) ? kTabStride : 0u)];
             ex = e.x;
             ey = e.y;
             n = P.direct ? 0 : floor_int(f_mul(bits_to_float<DT>(b), P.sc.c2));
@@ -389,54 +388,170 @@ __device__ __forceinline__ float2 fast_partial(const uint4 (&raw)[kLoads], float
     return make_float2(M, s);
 }
 
+// Shared-memory load of one table entry through its shared-window byte address.
+__device__ __forceinline__ float2 lds_f2(uint32_t a) {
+    float2 v;
+    asm("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t shared_addr(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// A lane block of kSub logits of a sampled row: piece(i) returns logits (i ^ sw) * PERP ..
+// + PERP - 1 of the block as one 16-byte piece (PERP = 16 / element size), bits(q) the raw bits
+// of logit q, those at or past V as -inf. GlobalSrc reads the row in global memory (16-byte
+// loads when the row allows them, `vec`, else logit by logit); SharedSrc reads the block's 128
+// bytes in shared memory, whose logits past V the caller has already overwritten with -inf.
+template <int DT>
+struct GlobalSrc {
+    static constexpr int kUnroll = 1;  // pieces per step of the table pass
+    const void* row;
+    long long e0;
+    int V;
+    bool vec;
+    __device__ __forceinline__ uint4 piece(int i) const {
+        constexpr int PERP = 16 / Geo<DT>::kBytes;
+        const long long e = e0 + (long long)i * PERP;
+        if (vec && e + PERP <= V)
+            return __ldca(reinterpret_cast<const uint4*>(static_cast<const char*>(row) + e * Geo<DT>::kBytes));
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (DT == 1) {
+                const uint32_t lo = e + 2 * j < V ? logit_bits<DT>(row, e + 2 * j) : 0xff80u;
+                const uint32_t hi = e + 2 * j + 1 < V ? logit_bits<DT>(row, e + 2 * j + 1) : 0xff80u;
+                w[j] = lo | (hi << 16);
+            } else {
+                w[j] = e + j < V ? logit_bits<DT>(row, e + j) : 0xff800000u;
+            }
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    __device__ __forceinline__ uint32_t bits(int q) const {
+        return e0 + q < V ? logit_bits<DT>(row, e0 + q) : neg_inf_bits<DT>();
+    }
+    __device__ __forceinline__ bool live() const { return e0 < V; }  // the block holds a logit
+};
+template <int DT>
+struct SharedSrc {
+    static constexpr int kUnroll = 1;
+    const unsigned char* base;  // the block's 128 bytes
+    int sw;
+    bool has;  // the block holds a logit
+    __device__ __forceinline__ bool live() const { return has; }
+    __device__ __forceinline__ uint4 piece(int i) const {
+        return *reinterpret_cast<const uint4*>(base + ((i ^ sw) << 4));
+    }
+    __device__ __forceinline__ uint32_t bits(int q) const {
+        return DT == 1 ? (uint32_t)reinterpret_cast<const unsigned short*>(base)[q]
+                       : reinterpret_cast<const uint32_t*>(base)[q];
+    }
+};
+
+// With nref at most kDirectMaxRef the direct table pass can sum in absolute terms: its
+// accumulator starts at 2^(nref+2) and stays below 2^(nref+8) <= 2^127.
+constexpr int kDirectMaxRef = 119;
+
+// Table indices of both bf16 logits of a word, as 16-bit halves: |z|'s offset from kTabMagLo
+// (taken modulo 2^16 without borrows between the halves) clamped to the zero entry kTabHalf,
+// plus kTabStride for a negative logit. `off` receives the unclamped offsets (a half >= kTabHalf:
+// outside the table's domain).
+__device__ __forceinline__ uint32_t tab_index2(uint32_t u, uint32_t& off) {
+    off = ((u | 0x80008000u) - kTabMagLo * 0x10001u) ^ 0x80008000u;
+    uint32_t c;
+    asm("min.u16x2 %0, %1, %2;" : "=r"(c) : "r"(off), "r"(kTabHalf * 0x10001u));
+    return c + ((u >> 15) & 0x00010001u) * kTabStride;
+}
+
+// Table pass over a bf16 lane block: the sum of exp(c z) / 2^nref over the logits inside the
+// table's domain, as a double-float; bit i of `rare` is set when piece i holds a logit outside
+// it (a zero entry stands in for it). KIND 0: the table holds exp(c z) itself and the pass adds
+// the entries on an accumulator biased by 2^(nref+2), scaling the sum by 2^-nref once at the
+// end; KIND 2: the table holds e with exp(c z) = e 2^n, n = floor(z c2), each entry scaled by
+// 2^(n - nref) on the way in (bias 4). The low and high logit of every word feed two independent
+// accumulators, renormalised after every piece. (The pass stays one piece per step: the hot
+// loop of the streaming kernel has to fit the instruction cache.)
+template <int KIND, typename Src>
+__device__ __forceinline__ dd table_pass(const Src& src, uint32_t tab, int nref, float c2,
+                                         unsigned& rare) {
+    const float bias = KIND == 0 ? pow2i(nref + 2) : kBias;
+    const float S = pow2i(-nref);
+    dd a0{bias, 0.0f}, a1{bias, 0.0f};
+    unsigned pieces = 0;
+#pragma unroll(Src::kUnroll)
+    for (int i = 0; i < kLoads; ++i) {
+        const uint4 v = src.piece(i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t omax = 0;  // per half: the largest offset of the piece
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t u = w[j];
+            uint32_t off;
+            const uint32_t ix = tab_index2(u, off);
+            asm("max.u16x2 %0, %1, %2;" : "=r"(omax) : "r"(omax), "r"(off));
+            float2 e0 = lds_f2(tab + (ix & 0xffffu) * 8u), e1 = lds_f2(tab + (ix >> 16) * 8u);
+            if (KIND == 2) {
+                const float s0 = pow2i(floor_int(f_mul(bf16_lo(u), c2)) - nref);
+                const float s1 = pow2i(floor_int(f_mul(bf16_hi(u), c2)) - nref);
+                e0 = make_float2(f_mul(e0.x, s0), f_mul(e0.y, s0));
+                e1 = make_float2(f_mul(e1.x, s1), f_mul(e1.y, s1));
+            }
+            acc_biased(a0, dd{e0.x, e0.y});
+            acc_biased(a1, dd{e1.x, e1.y});
+        }
+        if ((omax & 0xffffu) >= kTabHalf || (omax >> 16) >= kTabHalf) pieces |= 1u << i;
+        a0 = fast_two_sum(a0.hi, a0.lo);
+        a1 = fast_two_sum(a1.hi, a1.lo);
+    }
+    rare = pieces;
+    dd s = dd_add(fast_two_sum(f_sub(a0.hi, bias), a0.lo), fast_two_sum(f_sub(a1.hi, bias), a1.lo));
+    if (KIND == 0) s = dd{f_mul(s.hi, S), f_mul(s.lo, S)};
+    return s;
+}
+
 // Precise partials of one chunk of a row that will be sampled. Lane l stores the double-float
-// sum of exp(c z) / 2^nref over its block of kSub logits in sub_out[l]; lane 0 stores the chunk
-// total in *tot_out. nref = floor(m c2) for the chunk's largest logit m. The lane's block comes
-// from `src`: src.vec(i), i = 0..7, returns its eight 16-byte pieces in some order (only valid
-// when the block lies entirely below V, `full`), src.bits(q) the raw bits of its q-th logit.
+// sum of exp(c z) / 2^nref over its block of kSub logits (read through `src`, see GlobalSrc) in
+// sub_out[l]; lane 0 stores the chunk total in *tot_out. nref = floor(m c2) for the chunk's
+// largest logit m. Logits the table does not cover (all of them when there is no table) are
+// added by a second pass.
 template <int DT, typename Src>
-__device__ __forceinline__ void precise_core(const Src& src, bool full, long long e0, int V,
-                                             int lane, const PreciseCtx& P, float4* tot_out,
-                                             float4* sub_out) {
-    constexpr int SUB = Geo<DT>::kSub;
+__device__ __forceinline__ void precise_core(const Src& src, int lane, const PreciseCtx& P,
+                                             float4* tot_out, float4* sub_out) {
     // the block's largest logit (bf16: packed maxima; a NaN either comes out as the maximum or
     // lies outside the table's domain, and the second pass below reports it)
     float m = kNegInf;
     bool nan = false;
-    if (full) {
-        if (DT == 1) {
-            const uint4 q0 = src.vec(0);
-            __nv_bfloat162 mx = *reinterpret_cast<const __nv_bfloat162*>(&q0.x);
+    if (DT == 1) {
+        const uint4 v0 = src.piece(0);
+        __nv_bfloat162 mx[2];
+        mx[0] = *reinterpret_cast<const __nv_bfloat162*>(&v0.x);
+        mx[1] = *reinterpret_cast<const __nv_bfloat162*>(&v0.y);
+        mx[0] = __hmax2(mx[0], *reinterpret_cast<const __nv_bfloat162*>(&v0.z));
+        mx[1] = __hmax2(mx[1], *reinterpret_cast<const __nv_bfloat162*>(&v0.w));
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint4 q = i == 0 ? q0 : src.vec(i);
-                const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+        for (int i = 1; i < kLoads; ++i) {
+            const uint4 v = src.piece(i);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                for (int j = 0; j < 4; ++j) mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&w[j]));
-            }
-            const uint32_t mw = *reinterpret_cast<const uint32_t*>(&mx);
-            m = fmaxf(bf16_lo(mw), bf16_hi(mw));
-            nan = (bf16_lo(mw) != bf16_lo(mw)) | (bf16_hi(mw) != bf16_hi(mw));
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint4 q = src.vec(i);
-                const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float a = __uint_as_float(w[j]);
-                    m = fmaxf(m, a);
-                    nan |= (a != a);
-                }
-            }
+            for (int j = 0; j < 4; ++j)
+                mx[j & 1] = __hmax2(mx[j & 1], *reinterpret_cast<const __nv_bfloat162*>(&w[j]));
         }
+        const __nv_bfloat162 mm = __hmax2(mx[0], mx[1]);
+        const uint32_t mw = *reinterpret_cast<const uint32_t*>(&mm);
+        m = fmaxf(bf16_lo(mw), bf16_hi(mw));
+        nan = (bf16_lo(mw) != bf16_lo(mw)) | (bf16_hi(mw) != bf16_hi(mw));
     } else {
-#pragma unroll 1
-        for (int q = 0; q < SUB; ++q) {
-            if (e0 + q >= V) break;
-            const float a = bits_to_float<DT>(src.bits(q));
-            m = fmaxf(m, a);
-            nan |= (a != a);
+#pragma unroll
+        for (int i = 0; i < kLoads; ++i) {
+            const uint4 v = src.piece(i);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float a = __uint_as_float(w[j]);
+                m = fmaxf(m, a);
+                nan |= (a != a);
+            }
         }
     }
     m = warp_max(m);
@@ -453,88 +568,53 @@ __device__ __forceinline__ void precise_core(const Src& src, bool full, long lon
         return;
     }
     const int nref = floor_int(f_mul(m, P.sc.c2));
-    dd acc{kBias, 0.0f};
-    bool rare = false;  // logits outside the table's domain, added in a second pass below
-    const bool direct = DT == 1 && P.tab && P.direct && nref >= kDirectMinRef;
-    const bool general_tab = DT == 1 && P.tab && !P.direct;
-    // Table pass without branches: a logit outside the table's domain reads the zero entry
-    // kTabSize and is flagged for the second pass.
-    if (full && direct) {
-        const float S = pow2i(-nref);
+    dd sv{0.0f, 0.0f};
+    unsigned rare = src.live() ? (1u << kLoads) - 1 : 0u;  // pieces left to the second pass
+    bool covered = false;
+    if (DT == 1 && P.tab && src.live()) {
+        const uint32_t tab = shared_addr(P.tab);
+        covered = true;
+        if (!P.direct)
+            sv = table_pass<2>(src, tab, nref, P.sc.c2, rare);
+        else if (nref >= kDirectMinRef && nref <= kDirectMaxRef)
+            sv = table_pass<0>(src, tab, nref, P.sc.c2, rare);
+        else  // a chunk whose weights all lie below 2^-60, or above 2^119: the second pass alone
+            covered = false;
+    }
+    if (__any_sync(0xffffffffu, rare != 0) && rare) {
+        // second pass over the pieces of this lane's block with logits the table pass did not cover
+        constexpr int PERP = 16 / Geo<DT>::kBytes;
+        dd acc{kBias, 0.0f};
+        do {
+            const int i = __ffs(rare) - 1;
+            rare &= rare - 1;
+            const uint4 v = src.piece(i);
 #pragma unroll 1
-        for (int i = 0; i < 8; ++i) {
-            const uint4 q = src.vec(i);
-            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t b = (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xffffu);
-                const uint32_t off = (b & 0x7fffu) - kTabMagLo;
-                const bool in = off < kTabHalf;
-                rare |= !in;
-                const float2 e = P.tab[in ? off + (b >> 15) * kTabHalf : (uint32_t)kTabSize];
-                acc_biased(acc, dd{f_mul(e.x, S), f_mul(e.y, S)});
-            }
-            acc = fast_two_sum(acc.hi, acc.lo);  // keep the low word small
-        }
-    } else if (full && general_tab) {
-#pragma unroll 1
-        for (int i = 0; i < 8; ++i) {
-            const uint4 q = src.vec(i);
-            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t b = (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xffffu);
-                const uint32_t off = (b & 0x7fffu) - kTabMagLo;
-                const bool in = off < kTabHalf;
-                rare |= !in;
-                const float2 e = P.tab[in ? off + (b >> 15) * kTabHalf : (uint32_t)kTabSize];
-                const int n = floor_int(f_mul(bits_to_float<1>(b), P.sc.c2));
-                const float sc = pow2i(n - nref);
-                acc_biased(acc, dd{f_mul(e.x, sc), f_mul(e.y, sc)});
+            for (int q = 0; q < PERP; ++q) {
+                const int j = DT == 1 ? q >> 1 : q;
+                const uint32_t wj = j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+                const uint32_t b = DT == 1 ? ((q & 1) ? (wj >> 16) : (wj & 0xffffu)) : wj;
+                if (b == neg_inf_bits<DT>()) continue;
+                if (DT == 1 && covered && ((b & 0x7fffu) - kTabMagLo) < kTabHalf) continue;
+                acc_biased(acc, precise_weight<DT>(b, nref, P));
             }
             acc = fast_two_sum(acc.hi, acc.lo);
-        }
-    } else {
-        rare = true;
+        } while (rare);
+        sv = dd_add(sv, unbias(acc));
     }
-    if (__any_sync(0xffffffffu, rare) && rare) {
-        // second pass over this lane's block for the logits the table pass did not cover
-        const bool covered = full && (direct || general_tab);
-#pragma unroll 1
-        for (int q = 0; q < SUB; ++q) {
-            if (e0 + q >= V) break;
-            const uint32_t b = src.bits(q);
-            if (covered && ((b & 0x7fffu) - kTabMagLo) < kTabHalf) continue;
-            acc_biased(acc, precise_weight<DT>(b, nref, P));
-            if ((q & 7) == 7) acc = fast_two_sum(acc.hi, acc.lo);
-        }
-    }
-    const dd sv = unbias(acc);
     sub_out[lane] = pack_part(sv, nref);
     const dd total = warp_sum_dd(sv);
     if (lane == 0) *tot_out = pack_part(total, nref);
 }
 
-// Lane block read from global memory (cached in L1 for the second pass).
-template <int DT>
-struct GlobalBlock {
-    const uint4* blk;
-    const void* row;
-    long long e0;
-    __device__ __forceinline__ uint4 vec(int i) const { return __ldca(blk + i); }
-    __device__ __forceinline__ uint32_t bits(int q) const { return logit_bits<DT>(row, e0 + q); }
-};
-
+// Precise partials of chunk `chunk` of a row in global memory (cached in L1 for the second
+// pass): lane l's block of kSub logits from chunk * kChunk + l * kSub.
 template <int DT>
 __device__ __forceinline__ void precise_partials(const void* row, int V, bool vec, int chunk,
                                                  int lane, const PreciseCtx& P, float4* tot_out,
                                                  float4* sub_out) {
-    constexpr int SUB = Geo<DT>::kSub;
-    const long long e0 = (long long)chunk * Geo<DT>::kChunk + (long long)lane * SUB;
-    const GlobalBlock<DT> src{reinterpret_cast<const uint4*>(static_cast<const char*>(row) +
-                                                             e0 * Geo<DT>::kBytes),
-                              row, e0};
-    precise_core<DT>(src, vec && e0 + SUB <= V, e0, V, lane, P, tot_out, sub_out);
+    const long long e0 = (long long)chunk * Geo<DT>::kChunk + (long long)lane * Geo<DT>::kSub;
+    precise_core<DT>(GlobalSrc<DT>{row, e0, V, vec}, lane, P, tot_out, sub_out);
 }
 
 // ------------------------------------------------------------------------------------------

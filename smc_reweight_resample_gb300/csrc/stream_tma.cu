@@ -32,7 +32,7 @@ constexpr int kRing = kWarp;  // one slot per producer lane
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 constexpr size_t kSmemRing = (size_t)kRing * kChunkBytes;
-constexpr size_t kSmemTab = (size_t)kTabAlloc * sizeof(float2);
+constexpr size_t kSmemTab = (size_t)kTabSize * sizeof(float2);
 constexpr size_t kSmemBytes =
     kSmemRing + kSmemTab + sizeof(Exp2Table) + 2 * kRing * 8 + kRing * 8 + 16;
 constexpr uint32_t kTagNone = 0xffffffffu;  // slot never loaded
@@ -145,22 +145,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         "l"(src), "r"(bytes), "r"(bar), "l"(pol)
         : "memory");
 }
-
-// Lane block of a precise chunk from its shared-memory slot. The 16-byte pieces are read with an
-// XOR swizzle (piece i of lane l at (i ^ (l & 7)) * 16) so that each quarter-warp touches eight
-// different bank groups.
-template <int DT>
-struct SmemBlock {
-    const unsigned char* base;  // this lane's 128 bytes
-    int sw;
-    __device__ __forceinline__ uint4 vec(int i) const {
-        return *reinterpret_cast<const uint4*>(base + ((i ^ sw) << 4));
-    }
-    __device__ __forceinline__ uint32_t bits(int q) const {
-        return DT == 1 ? (uint32_t)reinterpret_cast<const unsigned short*>(base)[q]
-                       : reinterpret_cast<const uint32_t*>(base)[q];
-    }
-};
 
 // A producer lane: it owns slot `slot` and loads the block's chunks 32 * round + slot into it,
 // each once the consumer of the slot's previous chunk has handed the slot back, then tags the
@@ -368,14 +352,34 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                 if (lane == 0)
                     ws_ptr<float2>(p.ws, p.L.fast)[((size_t)s * p.slots + rs) * p.cpr + chunk] = fp;
             } else {
+                // a sampled row: lane l takes the contiguous block of kSub logits at l * 128
+                // bytes, its pieces read with an XOR swizzle (piece v ^ (l & 7)) so that each
+                // quarter-warp touches eight different bank groups; the slot goes back when the
+                // partials are done
                 constexpr int SUB = Geo<DT>::kSub;
                 const long long e0 = (long long)chunk * Geo<DT>::kChunk + (long long)lane * SUB;
-                const SmemBlock<DT> src{cbuf + lane * 128, lane & 7};
+                unsigned char* blk = ring + (size_t)slot * kChunkBytes + lane * 128;
+                const bool tail = chunk == p.cpr - 1;
+                if (tail) {
+                    // the row ends in this chunk: the lane overwrites its own logits past V with
+                    // -inf (the rest of the slot holds an older chunk)
+                    for (int q = 0; q < SUB; ++q)
+                        if (e0 + q >= p.R.V) {
+                            if (DT == 1) reinterpret_cast<unsigned short*>(blk)[q] = 0xff80u;
+                            else reinterpret_cast<uint32_t*>(blk)[q] = 0xff800000u;
+                        }
+                }
                 float4* tot = ws_ptr<float4>(p.ws, p.L.ddtot) + (size_t)(s * 2) * p.cpr + chunk;
                 float4* sub = ws_ptr<float4>(p.ws, p.L.ddsub) + ((size_t)(s * 2) * p.cpr + chunk) * kSubs;
-                precise_core<DT>(src, e0 + SUB <= p.R.V, e0, p.R.V, lane, P, tot, sub);
+                precise_core<DT>(SharedSrc<DT>{blk, lane & 7, e0 < p.R.V}, lane, P, tot, sub);
+                // the stores above must be ordered before the copy engine's next write to the
+                // slot: a proxy fence, and a releasing arrival
+                if (tail) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
-                if (lane == 0) mbar_arrive_relaxed(smem_u32(&empty[slot]));
+                if (lane == 0) {
+                    if (tail) mbar_arrive(smem_u32(&empty[slot]));
+                    else mbar_arrive_relaxed(smem_u32(&empty[slot]));
+                }
             }
         } else {
             __syncwarp();

@@ -16,7 +16,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     stream_kernel(const __grid_constant__ StreamParams p) {
     constexpr bool kPrecise = MODE != kModeSD;
     __shared__ Exp2Table sT;
-    __shared__ float2 sTab[(kPrecise && DT == 1) ? kTabAlloc : 1];
+    extern __shared__ __align__(16) float2 sTab[];  // kTabSize entries when the table is used
     load_exp2_table(p.T, sT);
     PreciseCtx P{p.sc_t, &sT, nullptr, p.ws, p.direct};
     if (kPrecise && DT == 1 && p.use_table) {
@@ -76,7 +76,10 @@ static cudaError_t launch_stream_t(const StreamParams& p, cudaStream_t st) {
     const long long cap = device_sm_count();
     int grid = (int)(want < cap ? want : cap);
     if (grid < 1) grid = 1;
-    kern<<<grid, kStreamThreads, 0, st>>>(p);
+    const size_t smem = (MODE != kModeSD && DT == 1 && p.use_table) ? (size_t)kTabSize * sizeof(float2) : 0;
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kStreamThreads, smem, st>>>(p);
     return cudaGetLastError();
 }
 
