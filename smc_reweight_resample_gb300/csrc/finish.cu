@@ -18,10 +18,13 @@
 
 namespace smcsd {
 
-constexpr int kFinishMaxWarps = 32;
+constexpr int kFinishMaxWarps = 16;
 
-// The fused step's group part, run by the block of the group's last particle: warp 0 computes the
-// ESS and resamples into shared memory, then all threads remap the group's page-table rows.
+// The fused step's group part for groups of at most kWarp particles, run by the block of the
+// group's last particle: warp 0 computes the ESS and resamples into shared memory (one particle
+// per lane), then all threads remap the group's page-table rows. Larger groups go to the
+// stand-alone resampling and page-table kernels after this pass: their code kept out of this
+// kernel, whose every SM runs it cold, keeps its instruction footprint small.
 __device__ __forceinline__ void group_part(const StreamParams& p, int g, int32_t* sAnc, int* sRes,
                                            int bar, int nthr) {
     const int N = p.N;
@@ -32,19 +35,9 @@ __device__ __forceinline__ void group_part(const StreamParams& p, int g, int32_t
         float* ess = p.ess ? p.ess + g : nullptr;
         int32_t* rs = p.resampled ? p.resampled + g : nullptr;
         const float U = __ldg(p.resample_uniforms + g);
-        bool res;
-        if (N <= kWarp * kResamplePer) {
-            int anc_reg[kResamplePer];
-            res = group_resample_small(lw, N, p.ess_threshold, U, anc, ess, rs, p.ws, lane, p.T, anc_reg);
-            const int per = (N + kWarp - 1) / kWarp;
-#pragma unroll
-            for (int q = 0; q < kResamplePer; ++q)
-                if (q < per && lane * per + q < N) sAnc[lane * per + q] = anc_reg[q];
-        } else {
-            res = group_resample_general(lw, N, p.ess_threshold, U, anc, ess, rs, p.ws, lane);
-            __syncwarp();
-            for (int j = lane; j < N; j += kWarp) sAnc[j] = __ldcg(anc + j);
-        }
+        int a[1];
+        const bool res = group_resample_small<1>(lw, N, p.ess_threshold, U, anc, ess, rs, p.ws, lane, p.T, a);
+        if (lane < N) sAnc[lane] = a[0];
         if (lane == 0) *sRes = res ? 1 : 0;
     }
     bar_sync(bar, nthr);
@@ -104,13 +97,13 @@ __global__ void __launch_bounds__(kFinishMaxWarps * kWarp)
             sd_seq_epilogue(p, s, ks, lane, sL, sX, sZ);
         } else {
             smc_particle_epilogue(p, s, lane, __shfl_sync(0xffffffffu, lw_old, 0), sL, sX, sZ);
-            if (MODE == kModeSMCStep) {
+            if (MODE == kModeSMCStep && p.N <= kWarp) {
                 const bool last = arrive_last(ws_ptr<unsigned>(p.ws, p.L.cnt_group) + s / p.N, (unsigned)p.N, lane);
                 if (lane == 0) sLast = last ? 1 : 0;
             }
         }
     }
-    if (MODE != kModeSMCStep) return;
+    if (MODE != kModeSMCStep || p.N > kWarp) return;
     bar_sync(bar, nthr);
     if (sLast) group_part(p, s / p.N, sAnc, &sRes, bar, nthr);
 }
@@ -135,7 +128,7 @@ template <int DT, int MODE>
 static cudaError_t launch_finish_t(const StreamParams& p, cudaStream_t st) {
     const int nw = p.slots < kFinishMaxWarps ? p.slots : kFinishMaxWarps;
     const size_t smem = (size_t)p.slots * (sizeof(float2) + sizeof(int) + sizeof(float)) +
-                        (MODE == kModeSMCStep ? (size_t)p.N * sizeof(int32_t) : 0);
+                        (MODE == kModeSMCStep ? (size_t)kWarp * sizeof(int32_t) : 0);
     auto kern = finish_kernel<DT, MODE>;
     if (smem > 48 * 1024) {
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

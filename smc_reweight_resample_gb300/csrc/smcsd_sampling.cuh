@@ -874,7 +874,7 @@ __device__ __forceinline__ int children_below(double C, double U, int N) {
     return (int)(j + 1);
 }
 
-// Resampling of a group of at most kWarp * kResamplePer particles with every weight computed
+// Resampling of a group of at most kWarp * PER particles with every weight computed
 // once and held in registers (lane l holds particles l*per .. l*per+per-1), in double-float
 // arithmetic on the FP32 pipes (about 2^-44 relative; this GPU's FP64 rate is far lower): the
 // weights w_i = exp(logw_i - max) from the double-float exp, ESS = W^2 / W2, the CDF
@@ -885,10 +885,11 @@ __device__ __forceinline__ int children_below(double C, double U, int N) {
 constexpr int kResamplePer = 4;
 
 // Value of register q of lane `src`, for a per-lane (src, q); `per` registers are live.
-__device__ __forceinline__ dd shfl_pick_dd(const dd (&v)[kResamplePer], int per, int src, int q) {
+template <int PER>
+__device__ __forceinline__ dd shfl_pick_dd(const dd (&v)[PER], int per, int src, int q) {
     dd r{0.0f, 0.0f};
 #pragma unroll
-    for (int q2 = 0; q2 < kResamplePer; ++q2) {
+    for (int q2 = 0; q2 < PER; ++q2) {
         if (q2 < per) {
             const float hi = __shfl_sync(0xffffffffu, v[q2].hi, src);
             const float lo = __shfl_sync(0xffffffffu, v[q2].lo, src);
@@ -898,19 +899,20 @@ __device__ __forceinline__ dd shfl_pick_dd(const dd (&v)[kResamplePer], int per,
     return r;
 }
 
+template <int PER>
 __device__ __forceinline__ bool group_resample_small(float* logw, int N, float thr, float U,
                                                      int32_t* anc, float* ess_out, int32_t* res_out,
                                                      void* ws, int lane, const Exp2Table& T,
-                                                     int (&anc_reg)[kResamplePer]) {
+                                                     int (&anc_reg)[PER]) {
     const int per = (N + kWarp - 1) / kWarp;
     const int i0 = min(lane * per, N), i1 = min(i0 + per, N);
 #pragma unroll
-    for (int q = 0; q < kResamplePer; ++q) anc_reg[q] = i0 + q;
-    float v[kResamplePer];
+    for (int q = 0; q < PER; ++q) anc_reg[q] = i0 + q;
+    float v[PER];
     bool bad = false;
     float m = kNegInf;
 #pragma unroll
-    for (int q = 0; q < kResamplePer; ++q) {
+    for (int q = 0; q < PER; ++q) {
         v[q] = kNegInf;
         if (i0 + q < i1) {
             v[q] = __ldcg(logw + i0 + q);
@@ -926,10 +928,10 @@ __device__ __forceinline__ bool group_resample_small(float* logw, int N, float t
         if (lane == 0 && res_out) *res_out = 0;
         return false;
     }
-    dd w[kResamplePer];
+    dd w[PER];
     dd loc{0.0f, 0.0f}, loc2{0.0f, 0.0f};
 #pragma unroll
-    for (int q = 0; q < kResamplePer; ++q) {
+    for (int q = 0; q < PER; ++q) {
         w[q] = dd{0.0f, 0.0f};
         if (q < per && i0 + q < i1 && v[q] > kNegInf) {
             const ddx e = exp_split(two_sum(v[q], -M), T);  // logw_i - max, exact as a double-float
@@ -951,10 +953,10 @@ __device__ __forceinline__ bool group_resample_small(float* logw, int N, float t
         return false;
     }
     const dd rW = dd_recip(W), rN = dd_recip(dd{(float)N, 0.0f});
-    dd C[kResamplePer], Vj[kResamplePer];
+    dd C[PER], Vj[PER];
     dd r = warp_exclusive_scan_dd(loc, lane);
 #pragma unroll
-    for (int q = 0; q < kResamplePer; ++q) {
+    for (int q = 0; q < PER; ++q) {
         C[q] = Vj[q] = dd{0.0f, 0.0f};
         if (q < per) {
             r = dd_add(r, w[q]);
@@ -965,10 +967,12 @@ __device__ __forceinline__ bool group_resample_small(float* logw, int N, float t
     }
     int top = 1;
     while (top * 2 <= N) top *= 2;
-    int cnt[kResamplePer] = {0, 0, 0, 0};
+    int cnt[PER];
+#pragma unroll
+    for (int q = 0; q < PER; ++q) cnt[q] = 0;
     for (int step = top; step > 0; step >>= 1) {
 #pragma unroll
-        for (int q = 0; q < kResamplePer; ++q) {
+        for (int q = 0; q < PER; ++q) {
             if (q < per) {
                 const int probe = cnt[q] + step - 1;
                 const int pc = min(probe, N - 1);
@@ -978,13 +982,13 @@ __device__ __forceinline__ bool group_resample_small(float* logw, int N, float t
         }
     }
 #pragma unroll
-    for (int q = 0; q < kResamplePer; ++q) {
+    for (int q = 0; q < PER; ++q) {
         anc_reg[q] = min(cnt[q], N - 1);
         if (i0 + q < i1) anc[i0 + q] = anc_reg[q];
     }
     __syncwarp();
 #pragma unroll
-    for (int q = 0; q < kResamplePer; ++q)
+    for (int q = 0; q < PER; ++q)
         if (i0 + q < i1) logw[i0 + q] = 0.0f;
     return true;
 }

@@ -96,8 +96,17 @@ static cudaError_t launch_stream_pass(const StreamParams& p, cudaStream_t st) {
 }
 
 cudaError_t launch_stream(const StreamParams& p, cudaStream_t st) {
-    const cudaError_t e = launch_stream_pass(p, st);
-    return e != cudaSuccess ? e : launch_finish(p, st);
+    cudaError_t e = launch_stream_pass(p, st);
+    if (e == cudaSuccess) e = launch_finish(p, st);
+    if (e != cudaSuccess || p.mode != kModeSMCStep || p.N <= kWarp) return e;
+    // groups too large for the finishing pass's one-warp group part
+    const ResampleParams rp{p.logw, p.G, p.N, p.ess_threshold, p.resample_uniforms, p.ancestors,
+                            p.ess, p.resampled, p.ws, p.T};
+    e = launch_resample(rp, st);
+    if (e != cudaSuccess || !p.table_in) return e;
+    const RemapParams mp{p.ancestors, p.resampled, p.G, p.N, p.table_in, p.table_out,
+                         p.pages_per_seq, p.refcount, p.num_pages, p.ws};
+    return launch_remap(mp, st);
 }
 
 }  // namespace smcsd
