@@ -8,15 +8,18 @@
 // compute the chunk's partial (fast or precise, smcsd_sampling.cuh) into the workspace, where
 // the finishing pass (finish.cu) picks the partials up. A fast chunk is copied into registers
 // and its slot handed back (a second mbarrier per slot) before the arithmetic, so that nearly
-// the whole ring stays in flight; a precise chunk, read twice, keeps its slot until done. Every
+// the whole ring stays in flight; a precise chunk, read from the slot twice, keeps it until done. Every
 // logit crosses HBM exactly once.
 //
 // Chunks are dealt from two lists, each round-robin over the B blocks: the precise chunks (the
 // rows that are sampled, one per particle) and the fast chunks (all other rows). Block b takes
-// chunks b, b+B, b+2B, ... of each list and interleaves them, one precise chunk to fslots fast
-// ones, so every block gets the same share of each kind spread evenly over the pass, without a
-// shared counter (a claim from one would put an atomic round trip on the producer's path).
-// The producer lane of slot j loads the block's local chunks 32 * round + j.
+// chunks b, b+B, b+2B, ... of the precise list and B-1-b, 2B-1-b, ... of the fast list (so the
+// blocks left with one precise chunk more get no extra fast chunk), puts the precise chunks the
+// fast ones cannot pair up first, then interleaves one precise chunk to fslots fast ones, and
+// ends on the fast chunks left over: every block gets the same share of each kind spread evenly
+// over the pass and finishes on cheap chunks, without a shared counter (a claim from one would
+// put an atomic round trip on the producer's path). The producer lane of slot j loads the
+// block's local chunks 32 * round + j.
 //
 // Every wait is bounded (about 2 s of wall time): a wait that runs out records
 // SMCSD_ERR_TIMEOUT in the workspace and the warp leaves; the producer, before it leaves,
@@ -165,31 +168,39 @@ __device__ __noinline__ void tma_producer(const StreamParams& p, unsigned char* 
     bool done = !active;
     unsigned streak = 0;  // failed polls in a row, and when the streak began
     unsigned long long t_streak = 0;
-    // this block's shares of the two lists and how they interleave: groups of one precise chunk
-    // and fslots fast ones while both last (phase 1, local chunks k < L1), then the rest of the
-    // longer list. Each lane tracks its k = q * m + r (m = fslots + 1) incrementally, in 32-bit
+    // This block's shares of the two lists and their order: the precise chunks the fast list
+    // cannot pair up first (phase 0, local chunks k < E), then groups of one precise chunk and
+    // fslots fast ones (phase 1, L1 chunks), then the fast chunks left over (phase 2), so that a
+    // block's last chunks are cheap ones. The fast list is dealt in reverse block order, so that
+    // the blocks holding one precise chunk more than others hold no extra fast chunk. Each lane
+    // tracks k1 = k - E = q * m + r (m = fslots + 1) incrementally once k1 >= 0, in 32-bit
     // arithmetic (every index is below 2^31), so a refill costs no division.
-    const uint32_t Bu = gridDim.x, bu = blockIdx.x, m = (uint32_t)p.fslots + 1u;
+    const uint32_t Bu = gridDim.x, bu = blockIdx.x, bf = Bu - 1u - bu, m = (uint32_t)p.fslots + 1u;
     const uint32_t Pb = p.n_precise > (long long)bu ? (uint32_t)((p.n_precise - 1 - bu) / Bu) + 1u : 0u;
-    const uint32_t Fb = p.n_fast > (long long)bu ? (uint32_t)((p.n_fast - 1 - bu) / Bu) + 1u : 0u;
+    const uint32_t Fb = p.n_fast > (long long)bf ? (uint32_t)((p.n_fast - 1 - bf) / Bu) + 1u : 0u;
     const uint32_t G1 = p.fslots > 0 ? min(Pb, Fb / (uint32_t)p.fslots) : 0u;
-    const uint32_t L1 = G1 * m, Fr = Fb - G1 * (uint32_t)p.fslots;
-    const uint32_t dq = kRing / m, dr = kRing % m;  // k += 32 moves q by dq and r by dr
-    uint32_t k = (uint32_t)slot, q = k / m, r = k % m;
+    const uint32_t E = Pb - G1, L1 = G1 * m;
+    const uint32_t dq = kRing / m, dr = kRing % m;  // k1 += 32 moves q by dq and r by dr
+    uint32_t k = (uint32_t)slot, q = 0, r = 0;
+    if (k >= E) {
+        q = (k - E) / m;
+        r = (k - E) % m;
+    }
     auto local_item = [&]() -> long long {  // tag item of local chunk k, or -1
         uint32_t j;
         bool precise;
-        if (k < L1) {
+        if (k < E) {
+            precise = true;
+            j = k;
+        } else if (k - E < L1) {
             precise = r == 0;
-            j = precise ? q : q * (uint32_t)p.fslots + r - 1u;
+            j = precise ? E + q : q * (uint32_t)p.fslots + r - 1u;
         } else {
-            const uint32_t k2 = k - L1;
-            precise = k2 >= Fr;
-            j = precise ? G1 + (k2 - Fr) : G1 * (uint32_t)p.fslots + k2;
-            if (precise && j >= Pb) return -1;
+            precise = false;
+            j = G1 * (uint32_t)p.fslots + (k - E - L1);
+            if (j >= Fb) return -1;
         }
-        const uint32_t g = j * Bu + bu;
-        return precise ? (long long)(g | 0x80000000u) : (long long)g;
+        return precise ? (long long)((j * Bu + bu) | 0x80000000u) : (long long)(j * Bu + bf);
     };
     bool moved = true;
     while (__any_sync(0xffffffffu, !done)) {
@@ -239,13 +250,18 @@ __device__ __noinline__ void tma_producer(const StreamParams& p, unsigned char* 
         }
         tag_store(tb, round * kRing + (uint32_t)slot, (c.valid && sane) ? (uint32_t)it : 0xffffffffu);
         ++round;
-        k += kRing;
-        q += dq;
-        r += dr;
-        if (r >= m) {
-            r -= m;
-            ++q;
+        if (k >= E) {
+            q += dq;
+            r += dr;
+            if (r >= m) {
+                r -= m;
+                ++q;
+            }
+        } else if (k + kRing >= E) {  // k1 turns non-negative: one division
+            q = (k + kRing - E) / m;
+            r = (k + kRing - E) % m;
         }
+        k += kRing;
     }
     // the copy of this lane's last chunk may still be in flight: wait for it before leaving
     if (round > 0) mbar_wait(fb, (round - 1) & 1u);

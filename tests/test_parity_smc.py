@@ -196,8 +196,12 @@ def test_smc_step_full_size(smcsd, cfg):
     assert first_div is None
 
 
-def test_fused_step_equals_separate_calls(smcsd):
-    cfg = small_cfg(20000)
+@pytest.mark.parametrize("GN", [(8, 16), (3, 48)], ids=["groups_of_16", "groups_of_48"])
+def test_fused_step_equals_separate_calls(smcsd, GN):
+    """The fused step equals reweight + resample + remap called one by one; groups of 48 take
+    the fused step's path for groups larger than one warp."""
+    G, N = GN
+    cfg = synth.SMCConfig("smc_small", G, N, 4, 20000, 3.0, 1.0, 1.0, 1.0, 256)
     S, K, V, G, N, P = cfg.S, cfg.K, cfg.V, cfg.G, cfg.N, cfg.pages_per_seq
     x = synth.smc_step_inputs(cfg, 3, 0)
     lw0 = np.random.default_rng(3).normal(0, 2, S).astype(np.float32)
