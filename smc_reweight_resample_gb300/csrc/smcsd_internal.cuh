@@ -85,7 +85,6 @@ struct SeqState {  // per-sequence hand-off between the SD kernels
 
 struct WsLayout {
     size_t flag;       // int32 error flag
-    size_t cnt_seq1;   // uint32 [S]  first pass
     size_t cnt_seq2;   // uint32 [S]  second pass (SD)
     size_t cnt_seq3;   // uint32 [S]  third pass (SD)
     size_t cnt_group;  // uint32 [S]
@@ -97,8 +96,6 @@ struct WsLayout {
     size_t rtot;       // float4 [S * cpr]              residual chunk totals (SD)
     size_t rsub;       // float4 [S * cpr * kSubs]      residual lane-block partials (SD)
     size_t seq;        // SeqState [S]
-    size_t rowL;       // float2 [S * (2K+1)] row normalisers log sum_i exp(c z_i), double-float
-    size_t zsel;       // float  [S * (2K+1)]  logit of the row at its draft token
     size_t tab;        // cached exp table: 4 tag words + kTabSize float2 (see setup_exp_table)
     size_t total;
 };
@@ -113,8 +110,6 @@ inline WsLayout ws_layout(int S, int K, int V) {
     size_t o = 0;
     L.flag = o;
     o = align256(o + 16);
-    L.cnt_seq1 = o;
-    o = align256(o + 4 * s);
     L.cnt_seq2 = o;
     o = align256(o + 4 * s);
     L.cnt_seq3 = o;
@@ -137,10 +132,6 @@ inline WsLayout ws_layout(int S, int K, int V) {
     o = align256(o + 16 * s * cpr * kSubs);
     L.seq = o;
     o = align256(o + sizeof(SeqState) * s);
-    L.rowL = o;
-    o = align256(o + 8 * s * (2 * k + 1));
-    L.zsel = o;
-    o = align256(o + 4 * s * (2 * k + 1));
     L.tab = o;
     o = align256(o + 16 + 8 * (size_t)kTabSize);
     L.total = o;
