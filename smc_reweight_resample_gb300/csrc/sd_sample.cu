@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(kSampleThreads) sd_rows_kernel(const __grid_co
         const void* rp = row_ptr<DT>(which == 0 ? p.R.tgt : p.R.drf, row, p.R.V);
         float4* tot = ws_ptr<float4>(p.ws, p.L.ddtot) + (size_t)(s * 2 + which) * cpr + chunk;
         float4* sub = ws_ptr<float4>(p.ws, p.L.ddsub) + ((size_t)(s * 2 + which) * cpr + chunk) * kSubs;
-        precise_partials<DT>(rp, p.R.V, p.vec, chunk, lane, P, tot, sub);
+        precise_partials<DT, true>(rp, p.R.V, p.vec, chunk, lane, P, tot, sub);
         const unsigned expected = (unsigned)((mode == 1 ? 2 : 1) * cpr);
         if (arrive_last(ws_ptr<unsigned>(p.ws, p.L.cnt_seq2) + s, expected, lane))
             sd_rows_epilogue<DT>(p, P, s, mode, lane);
@@ -198,18 +198,44 @@ __global__ void __launch_bounds__(kSampleThreads)
         const void* trp = row_ptr<DT>(p.R.tgt, __ldcg(&seq[s].trow), p.R.V);
         const void* drp = row_ptr<DT>(p.R.drf, __ldcg(&seq[s].drow), p.R.V);
         const ResidualCtx c = residual_ctx(seq + s);
-        // this lane's block of SUB logits, processed in quarters
+        // this lane's block of SUB logits: with 16-byte loads when both rows allow them (the
+        // next piece of each row in flight while the current one is weighed), else logit by logit
         const long long e0 = (long long)chunk * Geo<DT>::kChunk + (long long)lane * SUB;
         dd acc{kBias, 0.0f};
+        if (p.vec && __all_sync(0xffffffffu, e0 + SUB <= p.R.V)) {
+            constexpr int PERP = 16 / Geo<DT>::kBytes;
+            const uint4* bt = reinterpret_cast<const uint4*>(static_cast<const char*>(trp) + e0 * Geo<DT>::kBytes);
+            const uint4* bd = reinterpret_cast<const uint4*>(static_cast<const char*>(drp) + e0 * Geo<DT>::kBytes);
+            uint4 ct = __ldg(bt), cd = __ldg(bd);
 #pragma unroll 1
-        for (int q0 = 0; q0 < SUB; q0 += 16) {
+            for (int i = 0; i < kLoads; ++i) {
+                uint4 nt = ct, nd = cd;
+                if (i + 1 < kLoads) {
+                    nt = __ldg(bt + i + 1);
+                    nd = __ldg(bd + i + 1);
+                }
+                const uint32_t wt[4] = {ct.x, ct.y, ct.z, ct.w}, wd[4] = {cd.x, cd.y, cd.z, cd.w};
 #pragma unroll
-            for (int q = 0; q < 16; ++q) {
-                const long long e = e0 + q0 + q;
-                if (e < p.R.V)
-                    acc_biased(acc, residual_weight<DT>(logit_bits<DT>(trp, e), logit_bits<DT>(drp, e), c, P));
+                for (int q = 0; q < PERP; ++q) {
+                    const uint32_t xt = DT == 1 ? ((q & 1) ? (wt[q >> 1] >> 16) : (wt[q >> 1] & 0xffffu)) : wt[q];
+                    const uint32_t xd = DT == 1 ? ((q & 1) ? (wd[q >> 1] >> 16) : (wd[q >> 1] & 0xffffu)) : wd[q];
+                    acc_biased(acc, residual_weight<DT>(xt, xd, c, P));
+                }
+                acc = fast_two_sum(acc.hi, acc.lo);
+                ct = nt;
+                cd = nd;
             }
-            acc = fast_two_sum(acc.hi, acc.lo);
+        } else {
+#pragma unroll 1
+            for (int q0 = 0; q0 < SUB; q0 += 16) {
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const long long e = e0 + q0 + q;
+                    if (e < p.R.V)
+                        acc_biased(acc, residual_weight<DT>(logit_bits<DT>(trp, e), logit_bits<DT>(drp, e), c, P));
+                }
+                acc = fast_two_sum(acc.hi, acc.lo);
+            }
         }
         const dd sv = unbias(acc);
         float4* tot = ws_ptr<float4>(p.ws, p.L.rtot) + (size_t)s * cpr;

@@ -449,6 +449,16 @@ struct SharedSrc {
     }
 };
 
+// A lane block already in registers (pieces in natural order), for passes that load a block at
+// once; only piece() with indices known at compile time (fully unrolled loops) keeps it there.
+struct RegSrc {
+    static constexpr int kUnroll = kLoads;
+    uint4 v[kLoads];
+    bool has;
+    __device__ __forceinline__ uint4 piece(int i) const { return v[i]; }
+    __device__ __forceinline__ bool live() const { return has; }
+};
+
 // With nref at most kDirectMaxRef the direct table pass can sum in absolute terms: its
 // accumulator starts at 2^(nref+2) and stays below 2^(nref+8) <= 2^127.
 constexpr int kDirectMaxRef = 119;
@@ -514,10 +524,11 @@ __device__ __forceinline__ dd table_pass(const Src& src, uint32_t tab, int nref,
 // sum of exp(c z) / 2^nref over its block of kSub logits (read through `src`, see GlobalSrc) in
 // sub_out[l]; lane 0 stores the chunk total in *tot_out. nref = floor(m c2) for the chunk's
 // largest logit m. Logits the table does not cover (all of them when there is no table) are
-// added by a second pass.
-template <int DT, typename Src>
-__device__ __forceinline__ void precise_core(const Src& src, int lane, const PreciseCtx& P,
-                                             float4* tot_out, float4* sub_out) {
+// added by a second pass, which reads the pieces it needs through `again` (the same block).
+template <int DT, typename Src, typename Again>
+__device__ __forceinline__ void precise_core(const Src& src, const Again& again, int lane,
+                                             const PreciseCtx& P, float4* tot_out,
+                                             float4* sub_out) {
     // the block's largest logit (bf16: packed maxima; a NaN either comes out as the maximum or
     // lies outside the table's domain, and the second pass below reports it)
     float m = kNegInf;
@@ -588,7 +599,7 @@ __device__ __forceinline__ void precise_core(const Src& src, int lane, const Pre
         do {
             const int i = __ffs(rare) - 1;
             rare &= rare - 1;
-            const uint4 v = src.piece(i);
+            const uint4 v = again.piece(i);
 #pragma unroll 1
             for (int q = 0; q < PERP; ++q) {
                 const int j = DT == 1 ? q >> 1 : q;
@@ -607,26 +618,69 @@ __device__ __forceinline__ void precise_core(const Src& src, int lane, const Pre
     if (lane == 0) *tot_out = pack_part(total, nref);
 }
 
-// Precise partials of chunk `chunk` of a row in global memory (cached in L1 for the second
-// pass): lane l's block of kSub logits from chunk * kChunk + l * kSub.
-template <int DT>
+// Precise partials of chunk `chunk` of a row in global memory: lane l's block of kSub logits
+// from chunk * kChunk + l * kSub. With kRegs (and a 16-byte aligned row holding the whole
+// block) the block's eight 16-byte loads are all in flight at once (kept in L2 for a later pass)
+// and both passes run from registers; otherwise pieces are read as the passes go (cached in L1
+// for the second).
+template <int DT, bool kRegs = false>
 __device__ __forceinline__ void precise_partials(const void* row, int V, bool vec, int chunk,
                                                  int lane, const PreciseCtx& P, float4* tot_out,
                                                  float4* sub_out) {
     const long long e0 = (long long)chunk * Geo<DT>::kChunk + (long long)lane * Geo<DT>::kSub;
-    precise_core<DT>(GlobalSrc<DT>{row, e0, V, vec}, lane, P, tot_out, sub_out);
+    const GlobalSrc<DT> g{row, e0, V, vec};
+    if (kRegs && vec && __all_sync(0xffffffffu, e0 + Geo<DT>::kSub <= V)) {
+        RegSrc r;
+        const uint4* blk = reinterpret_cast<const uint4*>(static_cast<const char*>(row) + e0 * Geo<DT>::kBytes);
+#pragma unroll
+        for (int i = 0; i < kLoads; ++i) r.v[i] = __ldg(blk + i);
+        r.has = true;
+        precise_core<DT>(r, g, lane, P, tot_out, sub_out);
+    } else {
+        precise_core<DT>(g, g, lane, P, tot_out, sub_out);
+    }
 }
 
 // ------------------------------------------------------------------------------------------
 // row normalisers from fast partials
 // ------------------------------------------------------------------------------------------
 
+// One fast partial {m, s} into a lane's running normaliser state: mq = fl(m c2) of its largest
+// chunk so far, s the lane's sum relative to 2^mq, M its largest m. These three helpers spell
+// out every rounding (no contraction left to the compiler), so that every lane layout that
+// takes the same partials in the same order gets the same bits.
+__device__ __forceinline__ void lse_acc(float& mq, float& s, float& M, float2 v, float c2) {
+    const float pm = v.x, ps = v.y;
+    if (pm == kNegInf) return;
+    M = fmaxf(M, pm);
+    const float q = f_mul(pm, c2);
+    if (q > mq) {
+        s = fmaf(s, hw_exp2(f_sub(mq, q)), ps);
+        mq = q;
+    } else {
+        s = fmaf(ps, hw_exp2(f_sub(q, mq)), s);
+    }
+}
+// A lane's sum relative to 2^Q, Q = fl(Mb c2) for the row's largest m, Mb.
+__device__ __forceinline__ float lse_rescaled(float mq, float s, float Q) {
+    return (mq == kNegInf) ? 0.0f : f_mul(s, hw_exp2(f_sub(mq, Q)));
+}
+// The normaliser from the row's largest m and the lanes' rescaled sums added up: c M exactly,
+// plus the float log of the sum and the residual of fl(M c2).
+__device__ __forceinline__ dd lse_final(float Mb, float Ssum, const Scale& sc) {
+    if (Mb == kNegInf || !(Ssum > 0.0f)) return dd{__int_as_float(0x7fc00000), 0.0f};
+    const float Q = f_mul(Mb, sc.c2);
+    const float rQ = fmaf(Mb, sc.c2, -Q);  // exact residual of fl(M c2)
+    const dd cM = dd_mul_f(dd{sc.c_hi, sc.c_lo}, Mb);
+    return dd_add(cM, two_sum(logf(Ssum), f_mul(-rQ, SMCSD_LN2_HI)));
+}
+
 // Natural-log normaliser log sum_i exp(c z_i) of one row from its cpr fast partials, as a
-// double-float on every lane (hi = NaN for a row without mass): c M exactly, plus the float
-// log of the rescaled sum and the residual of fl(M c2). The partials' loads are all in flight
-// together.
+// double-float on every lane (hi = NaN for a row without mass). Lane l takes partials
+// l, l + 32, l + 64, ... in that order; the lanes' states meet in butterfly reductions. The
+// partials' loads are all in flight together.
 __device__ __forceinline__ dd row_lse_fast(const float2* part, int cpr, const Scale& sc, int lane) {
-    float mq = kNegInf, s = 0.0f, M = kNegInf;  // running fl(m c2) of the lane's largest chunk, its sum, max m
+    float mq = kNegInf, s = 0.0f, M = kNegInf;
     for (int c0 = 0; c0 < cpr; c0 += 4 * kWarp) {
         float2 v[4];
 #pragma unroll
@@ -635,27 +689,10 @@ __device__ __forceinline__ dd row_lse_fast(const float2* part, int cpr, const Sc
             v[j] = c < cpr ? ld_cg2(part + c) : make_float2(kNegInf, 0.0f);
         }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float pm = v[j].x, ps = v[j].y;
-            if (pm == kNegInf) continue;
-            M = fmaxf(M, pm);
-            const float q = pm * sc.c2;
-            if (q > mq) {
-                s = s * hw_exp2(mq - q) + ps;
-                mq = q;
-            } else {
-                s += ps * hw_exp2(q - mq);
-            }
-        }
+        for (int j = 0; j < 4; ++j) lse_acc(mq, s, M, v[j], sc.c2);
     }
     const float Mb = warp_max(M);
-    const float Q = Mb * sc.c2;
-    const float t = (mq == kNegInf) ? 0.0f : s * hw_exp2(mq - Q);
-    const float Ssum = warp_sum(t);
-    if (Mb == kNegInf || !(Ssum > 0.0f)) return dd{__int_as_float(0x7fc00000), 0.0f};
-    const float rQ = fmaf(Mb, sc.c2, -Q);  // exact residual of fl(M c2)
-    const dd cM = dd_mul_f(dd{sc.c_hi, sc.c_lo}, Mb);
-    return dd_add(cM, two_sum(logf(Ssum), -rQ * SMCSD_LN2_HI));
+    return lse_final(Mb, warp_sum(lse_rescaled(mq, s, f_mul(Mb, sc.c2))), sc);
 }
 
 // ------------------------------------------------------------------------------------------

@@ -387,7 +387,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                 }
                 float4* tot = ws_ptr<float4>(p.ws, p.L.ddtot) + (size_t)(s * 2) * p.cpr + chunk;
                 float4* sub = ws_ptr<float4>(p.ws, p.L.ddsub) + ((size_t)(s * 2) * p.cpr + chunk) * kSubs;
-                precise_core<DT>(SharedSrc<DT>{blk, lane & 7, e0 < p.R.V}, lane, P, tot, sub);
+                const SharedSrc<DT> src{blk, lane & 7, e0 < p.R.V};
+                precise_core<DT>(src, src, lane, P, tot, sub);
                 // the stores above must be ordered before the copy engine's next write to the
                 // slot: a proxy fence, and a releasing arrival
                 if (tail) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
