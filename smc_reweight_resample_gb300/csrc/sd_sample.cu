@@ -14,21 +14,37 @@
 
 namespace smcsd {
 
-constexpr int kSampleThreads = 512;
+constexpr int kSampleThreads = 256;  // three blocks per SM beside the 61 KB exp table
 
 struct ResidualCtx {
     int n_t, n_d;
-    dd inv_t, inv_d;
+    dd inv_t, inv_d;  // 1 / (row total in units of 2^n)
+    dd a_t, a_d;      // the same times 2^-n (exact), for the direct table
+    bool direct;      // both rows' weights come straight from a direct table
 };
 
-// max(0, p_i - q_i), p_i = exp(c zt) / Z_t, q_i = exp(c zd) / Z_d, from raw logit bits.
+// max(0, p_i - q_i), p_i = exp(c zt) / Z_t, q_i = exp(c zd) / Z_d, from raw logit bits. With a
+// direct table both weights are one table entry times a_t (a_d); when float estimates of p_i and
+// q_i (each within 2^-22 of the exact value) already put p_i below q_i, the result is 0 without
+// the double-float products.
 template <int DT>
 __device__ __forceinline__ dd residual_weight(uint32_t bt, uint32_t bd, const ResidualCtx& c,
                                               const PreciseCtx& P) {
-    dd pt = precise_weight<DT>(bt, c.n_t, P);
-    dd qd = precise_weight<DT>(bd, c.n_d, P);
-    if (pt.hi > 0.0f) pt = dd_mul(pt, c.inv_t);
-    if (qd.hi > 0.0f) qd = dd_mul(qd, c.inv_d);
+    dd pt, qd;
+    const uint32_t ot = (bt & 0x7fffu) - kTabMagLo, od = (bd & 0x7fffu) - kTabMagLo;
+    if (DT == 1 && c.direct && ot < kTabHalf && od < kTabHalf) {
+        const float2 et = P.tab[ot + ((bt & 0x8000u) ? kTabStride : 0u)];
+        const float2 ed = P.tab[od + ((bd & 0x8000u) ? kTabStride : 0u)];
+        const float pf = f_mul(et.x, c.a_t.hi), qf = f_mul(ed.x, c.a_d.hi);
+        if (pf < f_mul(qf, 1.0f - 0x1p-20f)) return dd{0.0f, 0.0f};
+        pt = dd_mul(dd{et.x, et.y}, c.a_t);
+        qd = dd_mul(dd{ed.x, ed.y}, c.a_d);
+    } else {
+        pt = precise_weight<DT>(bt, c.n_t, P);
+        qd = precise_weight<DT>(bd, c.n_d, P);
+        if (pt.hi > 0.0f) pt = dd_mul(pt, c.inv_t);
+        if (qd.hi > 0.0f) qd = dd_mul(qd, c.inv_d);
+    }
     dd d = two_sum(pt.hi, -qd.hi);
     d.lo = f_add(d.lo, f_sub(pt.lo, qd.lo));
     d = two_sum(d.hi, d.lo);
@@ -61,12 +77,20 @@ struct ResidualBlock {
     }
 };
 
-__device__ __forceinline__ ResidualCtx residual_ctx(const SeqState* st) {
+// The direct-table products need n in [kDirectMinRef, kResidualMaxRef], so that the scaled
+// reciprocals (and the products' low words) stay normal floats.
+constexpr int kResidualMaxRef = 90;
+__device__ __forceinline__ ResidualCtx residual_ctx(const SeqState* st, const PreciseCtx& P) {
     ResidualCtx c;
     c.n_t = __ldcg(&st->n_t);
     c.n_d = __ldcg(&st->n_d);
     c.inv_t = dd{__ldcg(&st->inv_t_hi), __ldcg(&st->inv_t_lo)};
     c.inv_d = dd{__ldcg(&st->inv_d_hi), __ldcg(&st->inv_d_lo)};
+    c.direct = P.tab && P.direct && c.n_t >= kDirectMinRef && c.n_t <= kResidualMaxRef &&
+               c.n_d >= kDirectMinRef && c.n_d <= kResidualMaxRef;
+    const float st_ = pow2i(-c.n_t), sd_ = pow2i(-c.n_d);
+    c.a_t = dd{f_mul(c.inv_t.hi, st_), f_mul(c.inv_t.lo, st_)};
+    c.a_d = dd{f_mul(c.inv_d.hi, sd_), f_mul(c.inv_d.lo, sd_)};
     return c;
 }
 
@@ -112,7 +136,7 @@ __device__ __noinline__ void sd_rows_epilogue(const SampleParams& p, const Preci
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kSampleThreads) sd_rows_kernel(const __grid_constant__ SampleParams p) {
+__global__ void __launch_bounds__(kSampleThreads, 3) sd_rows_kernel(const __grid_constant__ SampleParams p) {
     __shared__ Exp2Table sT;
     extern __shared__ __align__(16) float2 sTab[];  // kTabSize entries when the table is used
     load_exp2_table_s(p.T, sT);
@@ -172,7 +196,7 @@ __device__ __noinline__ void sd_residual_epilogue(const SampleParams& p, const P
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kSampleThreads)
+__global__ void __launch_bounds__(kSampleThreads, 3)
     sd_residual_kernel(const __grid_constant__ SampleParams p) {
     __shared__ Exp2Table sT;
     extern __shared__ __align__(16) float2 sTab[];  // kTabSize entries when the table is used
@@ -197,7 +221,7 @@ __global__ void __launch_bounds__(kSampleThreads)
         if (__ldcg(&seq[s].mode) != 1) continue;
         const void* trp = row_ptr<DT>(p.R.tgt, __ldcg(&seq[s].trow), p.R.V);
         const void* drp = row_ptr<DT>(p.R.drf, __ldcg(&seq[s].drow), p.R.V);
-        const ResidualCtx c = residual_ctx(seq + s);
+        const ResidualCtx c = residual_ctx(seq + s, P);
         // this lane's block of SUB logits: with 16-byte loads when both rows allow them (the
         // next piece of each row in flight while the current one is weighed), else logit by logit
         const long long e0 = (long long)chunk * Geo<DT>::kChunk + (long long)lane * SUB;
