@@ -170,6 +170,20 @@ __global__ void __launch_bounds__(kSampleThreads, 3) sd_rows_kernel(const __grid
     }
 }
 
+// The per-sequence epilogue of the rows pass when that pass ran as a pipelined stream: one warp
+// per sequence, a programmatic dependent of the stream (it waits for it before reading).
+template <int DT>
+__global__ void __launch_bounds__(256) sd_rows_finish_kernel(const __grid_constant__ SampleParams p) {
+    __shared__ Exp2Table sT;
+    load_exp2_table_s(p.T, sT);
+    const PreciseCtx P{p.sc, &sT, nullptr, p.ws, p.direct};
+    const int lane = threadIdx.x & 31;
+    const int s = (int)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    griddep_wait();
+    if (s >= p.R.S || seq_len(p.R, s, p.ws) < 0) return;
+    sd_rows_epilogue<DT>(p, P, s, __ldcg(&ws_ptr<SeqState>(p.ws, p.L.seq)[s].mode), lane);
+}
+
 template <int DT>
 __device__ __noinline__ void sd_residual_epilogue(const SampleParams& p, const PreciseCtx& P,
                                                   const ResidualCtx& c, int s, const void* trp,
@@ -292,8 +306,41 @@ static cudaError_t launch_sd_sample_t(const SampleParams& p, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k2<<<grid_for(k2, (long long)p.R.S * 2 * p.cpr, smem), kSampleThreads, smem, st>>>(p);
-    e = cudaGetLastError();
+    if (p.vec) {
+        // aligned rows: the rows pass as the pipelined stream (precise chunks only), then its
+        // per-sequence epilogue
+        StreamParams sp{};
+        sp.R = p.R;
+        sp.dtype = DT;
+        sp.vec = true;
+        sp.mode = kModeSDRows;
+        sp.sc_t = sp.sc_d = p.sc;
+        sp.use_table = p.use_table;
+        sp.direct = p.direct;
+        sp.T = p.T;
+        sp.ws = p.ws;
+        sp.L = p.L;
+        sp.cpr = p.cpr;
+        sp.slots = 2 * p.R.K + 1;
+        sp.div_cpr = make_fastdiv((uint32_t)p.cpr);
+        e = launch_stream_tma(sp, st);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3((unsigned)((p.R.S + 7) / 8));
+        cfg.blockDim = dim3(256);
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        SampleParams q = p;
+        void* args[] = {&q};
+        e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(sd_rows_finish_kernel<DT>), args);
+    } else {
+        k2<<<grid_for(k2, (long long)p.R.S * 2 * p.cpr, smem), kSampleThreads, smem, st>>>(p);
+        e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return e;
     k3<<<grid_for(k3, (long long)p.R.S * p.cpr, smem), kSampleThreads, smem, st>>>(p);
     return cudaGetLastError();

@@ -209,6 +209,34 @@ __device__ __forceinline__ ChunkRef chunk_ref_two_list(const StreamParams& p, ui
     return c;
 }
 
+// Chunk of the SD final-token pass (kModeSDRows): precise item i (high bit set) is chunk i % cpr
+// of row `which` = (i / cpr) % 2 of sequence i / (2 cpr) (p.div_seq divides by 2 cpr here): the
+// sequence's target row to draw from (which 0) or its draft row (which 1, needed only for a
+// residual draw). With `rows` the row is looked up in the hand-off state, and a draft row that is
+// not needed (or a sequence that is not valid) makes the item invalid; without, only the indices
+// are decoded. `slot` carries `which`.
+__device__ __forceinline__ ChunkRef chunk_ref_sd_rows(const StreamParams& p, uint32_t tag_item, bool rows) {
+    ChunkRef c;
+    const uint32_t i = tag_item & 0x7fffffffu;
+    c.s = (int)fast_div(i, p.div_seq);
+    const uint32_t rem = i - (uint32_t)c.s * p.div_seq.d;
+    const int which = rem >= (uint32_t)p.cpr ? 1 : 0;
+    c.chunk = (int)rem - which * p.cpr;
+    c.slot = which;
+    c.ks = 0;
+    c.is_draft = which == 1;
+    c.valid = true;
+    c.row = 0;
+    if (rows) {
+        const int ks = seq_len(p.R, c.s, p.ws);
+        const SeqState* st = ws_ptr<SeqState>(p.ws, p.L.seq) + c.s;
+        const int mode = ks >= 0 ? __ldcg(&st->mode) : 0;
+        c.valid = ks >= 0 && !(which == 1 && mode == 0);
+        c.row = c.valid ? (which ? __ldcg(&st->drow) : __ldcg(&st->trow)) : 0;
+    }
+    return c;
+}
+
 // Within a sequence the rows come bonus row first (position 0 is row slot 2ks, position q > 0 is
 // slot q - 1), so that the bonus row's draw, the longest row epilogue, overlaps the streaming of
 // the sequence's other rows instead of following its last chunk.

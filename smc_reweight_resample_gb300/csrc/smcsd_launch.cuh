@@ -6,7 +6,9 @@
 
 namespace smcsd {
 
-enum StreamMode { kModeSD = 0, kModeSMC = 1, kModeSMCStep = 2 };
+// kModeSDRows: the SD final-token pass over the row (pair) each sequence draws from, all chunks
+// precise, rows looked up in the hand-off state the SD epilogue wrote.
+enum StreamMode { kModeSD = 0, kModeSMC = 1, kModeSMCStep = 2, kModeSDRows = 3 };
 
 // One streaming pass over all logits rows (SD first pass, SMC reweight, fused SMC step).
 struct StreamParams {

@@ -154,7 +154,7 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 // slot with the block-local sequence number k = 32 * round + slot and the chunk's index. A lane out
 // of chunks tags its slot kTagDone. The lanes poll their slots together (one non-blocking test per
 // lane per pass), so no lane spins alone while the others wait on it.
-template <int DT>
+template <int DT, bool kSDRows>
 __device__ __noinline__ void tma_producer(const StreamParams& p, unsigned char* ring,
                                           uint64_t* full, uint64_t* empty,
                                           unsigned long long* tag, unsigned* n_done, int slot,
@@ -229,7 +229,8 @@ __device__ __noinline__ void tma_producer(const StreamParams& p, unsigned char* 
             done = true;
             continue;
         }
-        const ChunkRef c = chunk_ref_two_list(p, (uint32_t)it);
+        const ChunkRef c = kSDRows ? chunk_ref_sd_rows(p, (uint32_t)it, true)
+                                   : chunk_ref_two_list(p, (uint32_t)it);
         const long long off = (long long)c.chunk * kChunkBytes;
         const long long left = row_bytes - off;
         const uint32_t bytes = (uint32_t)(left < kChunkBytes ? left : kChunkBytes);
@@ -296,7 +297,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     if (threadIdx.x == 0) griddep_launch_dependents();
     if (warp < kTmaProducers) {
         constexpr int kPer = kRing / kTmaProducers;
-        tma_producer<DT>(p, ring, full, empty, tag, n_done, warp * kPer + (lane % kPer), lane < kPer);
+        tma_producer<DT, MODE == kModeSDRows>(p, ring, full, empty, tag, n_done, warp * kPer + (lane % kPer), lane < kPer);
         return;
     }
 
@@ -338,14 +339,15 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         const uint32_t item = (uint32_t)seen;  // 0xffffffff: a chunk with nothing to load
         ChunkRef c{};
         c.valid = false;
-        if (item != 0xffffffffu) c = chunk_ref_two_list(p, item);
+        if (item != 0xffffffffu)
+            c = MODE == kModeSDRows ? chunk_ref_sd_rows(p, item, false) : chunk_ref_two_list(p, item);
         const int s = c.valid ? c.s : -1, rs = c.slot, ks = c.ks, chunk = c.chunk;
         const bool is_draft = c.is_draft;
         const unsigned char* cbuf = ring + (size_t)slot * kChunkBytes;
         const bool sane = s < 0 || (check_ok(p.ws, chunk >= 0 && chunk < p.cpr, -111, chunk) &&
-                                    check_ok(p.ws, rs >= 0 && rs < p.slots, -112, rs));
+                                    check_ok(p.ws, rs >= 0 && rs < (MODE == kModeSDRows ? 2 : p.slots), -112, rs));
         if (s >= 0 && sane) {
-            if (!kPrecise || rs != 2 * ks) {
+            if (MODE != kModeSDRows && (!kPrecise || rs != 2 * ks)) {
                 uint4 raw[kLoads];
 #pragma unroll
                 for (int v = 0; v < kLoads; ++v)
@@ -385,8 +387,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                             else reinterpret_cast<uint32_t*>(blk)[q] = 0xff800000u;
                         }
                 }
-                float4* tot = ws_ptr<float4>(p.ws, p.L.ddtot) + (size_t)(s * 2) * p.cpr + chunk;
-                float4* sub = ws_ptr<float4>(p.ws, p.L.ddsub) + ((size_t)(s * 2) * p.cpr + chunk) * kSubs;
+                // sampled rows sit at 2s (SMC: the bonus row; SD: the target row) and 2s + 1
+                const size_t prow = (size_t)(s * 2 + (MODE == kModeSDRows ? rs : 0));
+                float4* tot = ws_ptr<float4>(p.ws, p.L.ddtot) + prow * p.cpr + chunk;
+                float4* sub = ws_ptr<float4>(p.ws, p.L.ddsub) + (prow * p.cpr + chunk) * kSubs;
                 const SharedSrc<DT> src{blk, lane & 7, e0 < p.R.V};
                 precise_core<DT>(src, src, lane, P, tot, sub);
                 // the stores above must be ordered before the copy engine's next write to the
@@ -409,12 +413,21 @@ template <int DT, int MODE>
 static cudaError_t launch_tma_t(const StreamParams& p0, cudaStream_t st) {
     auto kern = stream_tma_kernel<DT, MODE>;
     StreamParams p = p0;
-    // the sampled rows (one per particle) form the precise list; in SD mode every row is fast
-    const bool sampled = MODE != kModeSD;
-    p.fslots = sampled ? p.slots - 1 : p.slots;
-    p.n_precise = sampled ? (long long)p.R.S * p.cpr : 0;
-    p.n_fast = (long long)p.R.S * p.fslots * p.cpr;
-    p.div_fseq = make_fastdiv((uint32_t)(p.fslots > 0 ? p.fslots * p.cpr : 1));
+    if (MODE == kModeSDRows) {
+        // two rows per sequence (the second only when its draw needs it), all precise
+        p.fslots = 0;
+        p.n_precise = (long long)p.R.S * 2 * p.cpr;
+        p.n_fast = 0;
+        p.div_fseq = make_fastdiv(1u);
+        p.div_seq = make_fastdiv((uint32_t)(2 * p.cpr));
+    } else {
+        // the sampled rows (one per particle) form the precise list; in SD mode every row is fast
+        const bool sampled = MODE != kModeSD;
+        p.fslots = sampled ? p.slots - 1 : p.slots;
+        p.n_precise = sampled ? (long long)p.R.S * p.cpr : 0;
+        p.n_fast = (long long)p.R.S * p.fslots * p.cpr;
+        p.div_fseq = make_fastdiv((uint32_t)(p.fslots > 0 ? p.fslots * p.cpr : 1));
+    }
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -427,6 +440,8 @@ static cudaError_t launch_tma_t(const StreamParams& p0, cudaStream_t st) {
 }
 
 cudaError_t launch_stream_tma(const StreamParams& p, cudaStream_t st) {
+    if (p.mode == kModeSDRows)
+        return p.dtype == 0 ? launch_tma_t<0, kModeSDRows>(p, st) : launch_tma_t<1, kModeSDRows>(p, st);
     if (p.dtype == 0) {
         if (p.mode == kModeSD) return launch_tma_t<0, kModeSD>(p, st);
         if (p.mode == kModeSMC) return launch_tma_t<0, kModeSMC>(p, st);
