@@ -10,46 +10,11 @@
 //   epilogue draws the correction token (or falls back to p at the same row if the residual
 //   has no mass).
 // Both passes re-read one or two rows per sequence, which the first pass has just streamed.
-#include "smcsd_launch.cuh"
+#include "smcsd_epilogue.cuh"
 
 namespace smcsd {
 
 constexpr int kSampleThreads = 256;  // three blocks per SM beside the 61 KB exp table
-
-struct ResidualCtx {
-    int n_t, n_d;
-    dd inv_t, inv_d;  // 1 / (row total in units of 2^n)
-    dd a_t, a_d;      // the same times 2^-n (exact), for the direct table
-    bool direct;      // both rows' weights come straight from a direct table
-};
-
-// max(0, p_i - q_i), p_i = exp(c zt) / Z_t, q_i = exp(c zd) / Z_d, from raw logit bits. With a
-// direct table both weights are one table entry times a_t (a_d); when float estimates of p_i and
-// q_i (each within 2^-22 of the exact value) already put p_i below q_i, the result is 0 without
-// the double-float products.
-template <int DT>
-__device__ __forceinline__ dd residual_weight(uint32_t bt, uint32_t bd, const ResidualCtx& c,
-                                              const PreciseCtx& P) {
-    dd pt, qd;
-    const uint32_t ot = (bt & 0x7fffu) - kTabMagLo, od = (bd & 0x7fffu) - kTabMagLo;
-    if (DT == 1 && c.direct && ot < kTabHalf && od < kTabHalf) {
-        const float2 et = P.tab[ot + ((bt & 0x8000u) ? kTabStride : 0u)];
-        const float2 ed = P.tab[od + ((bd & 0x8000u) ? kTabStride : 0u)];
-        const float pf = f_mul(et.x, c.a_t.hi), qf = f_mul(ed.x, c.a_d.hi);
-        if (pf < f_mul(qf, 1.0f - 0x1p-20f)) return dd{0.0f, 0.0f};
-        pt = dd_mul(dd{et.x, et.y}, c.a_t);
-        qd = dd_mul(dd{ed.x, ed.y}, c.a_d);
-    } else {
-        pt = precise_weight<DT>(bt, c.n_t, P);
-        qd = precise_weight<DT>(bd, c.n_d, P);
-        if (pt.hi > 0.0f) pt = dd_mul(pt, c.inv_t);
-        if (qd.hi > 0.0f) qd = dd_mul(qd, c.inv_d);
-    }
-    dd d = two_sum(pt.hi, -qd.hi);
-    d.lo = f_add(d.lo, f_sub(pt.lo, qd.lo));
-    d = two_sum(d.hi, d.lo);
-    return d.hi > 0.0f ? d : dd{0.0f, 0.0f};
-}
 
 template <int DT>
 struct ResidualBlock {
@@ -77,22 +42,6 @@ struct ResidualBlock {
     }
 };
 
-// The direct-table products need n in [kDirectMinRef, kResidualMaxRef], so that the scaled
-// reciprocals (and the products' low words) stay normal floats.
-constexpr int kResidualMaxRef = 90;
-__device__ __forceinline__ ResidualCtx residual_ctx(const SeqState* st, const PreciseCtx& P) {
-    ResidualCtx c;
-    c.n_t = __ldcg(&st->n_t);
-    c.n_d = __ldcg(&st->n_d);
-    c.inv_t = dd{__ldcg(&st->inv_t_hi), __ldcg(&st->inv_t_lo)};
-    c.inv_d = dd{__ldcg(&st->inv_d_hi), __ldcg(&st->inv_d_lo)};
-    c.direct = P.tab && P.direct && c.n_t >= kDirectMinRef && c.n_t <= kResidualMaxRef &&
-               c.n_d >= kDirectMinRef && c.n_d <= kResidualMaxRef;
-    const float st_ = pow2i(-c.n_t), sd_ = pow2i(-c.n_d);
-    c.a_t = dd{f_mul(c.inv_t.hi, st_), f_mul(c.inv_t.lo, st_)};
-    c.a_d = dd{f_mul(c.inv_d.hi, sd_), f_mul(c.inv_d.lo, sd_)};
-    return c;
-}
 
 __device__ __forceinline__ void load_exp2_table_s(const Exp2Table& src, Exp2Table& dst) {
     for (int i = threadIdx.x; i < 32; i += blockDim.x) {
@@ -209,6 +158,25 @@ __device__ __noinline__ void sd_residual_epilogue(const SampleParams& p, const P
     }
 }
 
+// The per-sequence residual draw when the residual pass ran as a pipelined stream: one warp per
+// sequence that draws a correction token, a programmatic dependent of the stream.
+template <int DT>
+__global__ void __launch_bounds__(256) sd_residual_finish_kernel(const __grid_constant__ SampleParams p) {
+    __shared__ Exp2Table sT;
+    load_exp2_table_s(p.T, sT);
+    const PreciseCtx P{p.sc, &sT, nullptr, p.ws, p.direct};
+    const int lane = threadIdx.x & 31;
+    const int s = (int)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    griddep_wait();
+    if (s >= p.R.S || seq_len(p.R, s, p.ws) < 0) return;
+    const SeqState* seq = ws_ptr<SeqState>(p.ws, p.L.seq);
+    if (__ldcg(&seq[s].mode) != 1) return;
+    const ResidualCtx c = residual_ctx(seq + s, P);
+    const void* trp = row_ptr<DT>(p.R.tgt, __ldcg(&seq[s].trow), p.R.V);
+    const void* drp = row_ptr<DT>(p.R.drf, __ldcg(&seq[s].drow), p.R.V);
+    sd_residual_epilogue<DT>(p, P, c, s, trp, drp, lane);
+}
+
 template <int DT>
 __global__ void __launch_bounds__(kSampleThreads, 3)
     sd_residual_kernel(const __grid_constant__ SampleParams p) {
@@ -298,6 +266,22 @@ static int grid_for(Kern kern, long long warps_needed, size_t smem) {
     return (int)(g < 1 ? 1 : g);
 }
 
+// One warp per sequence (8 per block), launched as a programmatic dependent of the stream before.
+static cudaError_t launch_warp_per_seq(const void* kern, const SampleParams& p, cudaStream_t st) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)((p.R.S + 7) / 8));
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    SampleParams q = p;
+    void* args[] = {&q};
+    return cudaLaunchKernelExC(&cfg, kern, args);
+}
+
 template <int DT>
 static cudaError_t launch_sd_sample_t(const SampleParams& p, cudaStream_t st) {
     const size_t smem = (DT == 1 && p.use_table) ? (size_t)kTabSize * sizeof(float2) : 0;
@@ -307,13 +291,12 @@ static cudaError_t launch_sd_sample_t(const SampleParams& p, cudaStream_t st) {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (p.vec) {
-        // aligned rows: the rows pass as the pipelined stream (precise chunks only), then its
-        // per-sequence epilogue
+        // aligned rows: the rows pass and the residual pass as the pipelined stream, each
+        // followed by its per-sequence epilogue as a programmatic dependent
         StreamParams sp{};
         sp.R = p.R;
         sp.dtype = DT;
         sp.vec = true;
-        sp.mode = kModeSDRows;
         sp.sc_t = sp.sc_d = p.sc;
         sp.use_table = p.use_table;
         sp.direct = p.direct;
@@ -323,24 +306,17 @@ static cudaError_t launch_sd_sample_t(const SampleParams& p, cudaStream_t st) {
         sp.cpr = p.cpr;
         sp.slots = 2 * p.R.K + 1;
         sp.div_cpr = make_fastdiv((uint32_t)p.cpr);
+        sp.mode = kModeSDRows;
         e = launch_stream_tma(sp, st);
+        if (e == cudaSuccess) e = launch_warp_per_seq(reinterpret_cast<const void*>(sd_rows_finish_kernel<DT>), p, st);
         if (e != cudaSuccess) return e;
-        cudaLaunchConfig_t cfg{};
-        cfg.gridDim = dim3((unsigned)((p.R.S + 7) / 8));
-        cfg.blockDim = dim3(256);
-        cfg.stream = st;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        SampleParams q = p;
-        void* args[] = {&q};
-        e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(sd_rows_finish_kernel<DT>), args);
-    } else {
-        k2<<<grid_for(k2, (long long)p.R.S * 2 * p.cpr, smem), kSampleThreads, smem, st>>>(p);
-        e = cudaGetLastError();
+        sp.mode = kModeSDResidual;
+        e = launch_stream_tma(sp, st);
+        if (e == cudaSuccess) e = launch_warp_per_seq(reinterpret_cast<const void*>(sd_residual_finish_kernel<DT>), p, st);
+        return e;
     }
+    k2<<<grid_for(k2, (long long)p.R.S * 2 * p.cpr, smem), kSampleThreads, smem, st>>>(p);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     k3<<<grid_for(k3, (long long)p.R.S * p.cpr, smem), kSampleThreads, smem, st>>>(p);
     return cudaGetLastError();

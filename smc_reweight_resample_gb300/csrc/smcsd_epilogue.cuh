@@ -209,6 +209,62 @@ __device__ __forceinline__ ChunkRef chunk_ref_two_list(const StreamParams& p, ui
     return c;
 }
 
+// ------------------------------------------------------------------------------------------
+// SD residual weights (the residual pass and the residual draw)
+// ------------------------------------------------------------------------------------------
+
+struct ResidualCtx {
+    int n_t, n_d;
+    dd inv_t, inv_d;  // 1 / (row total in units of 2^n)
+    dd a_t, a_d;      // the same times 2^-n (exact), for the direct table
+    bool direct;      // both rows' weights come straight from a direct table
+};
+
+// max(0, p_i - q_i), p_i = exp(c zt) / Z_t, q_i = exp(c zd) / Z_d, from raw logit bits. With a
+// direct table both weights are one table entry times a_t (a_d); when float estimates of p_i and
+// q_i (each within 2^-22 of the exact value) already put p_i below q_i, the result is 0 without
+// the double-float products.
+template <int DT>
+__device__ __forceinline__ dd residual_weight(uint32_t bt, uint32_t bd, const ResidualCtx& c,
+                                              const PreciseCtx& P) {
+    dd pt, qd;
+    const uint32_t ot = (bt & 0x7fffu) - kTabMagLo, od = (bd & 0x7fffu) - kTabMagLo;
+    if (DT == 1 && c.direct && ot < kTabHalf && od < kTabHalf) {
+        const float2 et = P.tab[ot + ((bt & 0x8000u) ? kTabStride : 0u)];
+        const float2 ed = P.tab[od + ((bd & 0x8000u) ? kTabStride : 0u)];
+        const float pf = f_mul(et.x, c.a_t.hi), qf = f_mul(ed.x, c.a_d.hi);
+        if (pf < f_mul(qf, 1.0f - 0x1p-20f)) return dd{0.0f, 0.0f};
+        pt = dd_mul(dd{et.x, et.y}, c.a_t);
+        qd = dd_mul(dd{ed.x, ed.y}, c.a_d);
+    } else {
+        pt = precise_weight<DT>(bt, c.n_t, P);
+        qd = precise_weight<DT>(bd, c.n_d, P);
+        if (pt.hi > 0.0f) pt = dd_mul(pt, c.inv_t);
+        if (qd.hi > 0.0f) qd = dd_mul(qd, c.inv_d);
+    }
+    dd d = two_sum(pt.hi, -qd.hi);
+    d.lo = f_add(d.lo, f_sub(pt.lo, qd.lo));
+    d = two_sum(d.hi, d.lo);
+    return d.hi > 0.0f ? d : dd{0.0f, 0.0f};
+}
+
+// The direct-table products need n in [kDirectMinRef, kResidualMaxRef], so that the scaled
+// reciprocals (and the products' low words) stay normal floats.
+constexpr int kResidualMaxRef = 90;
+__device__ __forceinline__ ResidualCtx residual_ctx(const SeqState* st, const PreciseCtx& P) {
+    ResidualCtx c;
+    c.n_t = __ldcg(&st->n_t);
+    c.n_d = __ldcg(&st->n_d);
+    c.inv_t = dd{__ldcg(&st->inv_t_hi), __ldcg(&st->inv_t_lo)};
+    c.inv_d = dd{__ldcg(&st->inv_d_hi), __ldcg(&st->inv_d_lo)};
+    c.direct = P.tab && P.direct && c.n_t >= kDirectMinRef && c.n_t <= kResidualMaxRef &&
+               c.n_d >= kDirectMinRef && c.n_d <= kResidualMaxRef;
+    const float st_ = pow2i(-c.n_t), sd_ = pow2i(-c.n_d);
+    c.a_t = dd{f_mul(c.inv_t.hi, st_), f_mul(c.inv_t.lo, st_)};
+    c.a_d = dd{f_mul(c.inv_d.hi, sd_), f_mul(c.inv_d.lo, sd_)};
+    return c;
+}
+
 // Chunk of the SD final-token pass (kModeSDRows): precise item i (high bit set) is chunk i % cpr
 // of row `which` = (i / cpr) % 2 of sequence i / (2 cpr) (p.div_seq divides by 2 cpr here): the
 // sequence's target row to draw from (which 0) or its draft row (which 1, needed only for a
@@ -232,6 +288,31 @@ __device__ __forceinline__ ChunkRef chunk_ref_sd_rows(const StreamParams& p, uin
         const SeqState* st = ws_ptr<SeqState>(p.ws, p.L.seq) + c.s;
         const int mode = ks >= 0 ? __ldcg(&st->mode) : 0;
         c.valid = ks >= 0 && !(which == 1 && mode == 0);
+        c.row = c.valid ? (which ? __ldcg(&st->drow) : __ldcg(&st->trow)) : 0;
+    }
+    return c;
+}
+
+// Half item of the SD residual pass (kModeSDResidual): item i (high bit set) is the target
+// (i even) or draft (i odd) chunk of pair i >> 1 = sequence s's chunk `chunk` (pair = s * cpr +
+// chunk). With `rows` the row is looked up in the hand-off state, and a sequence that does not
+// draw a correction token (or is not valid) makes the item invalid. `slot` carries which row.
+__device__ __forceinline__ ChunkRef chunk_ref_sd_residual(const StreamParams& p, uint32_t tag_item, bool rows) {
+    ChunkRef c;
+    const uint32_t i = tag_item & 0x7fffffffu;
+    const int which = (int)(i & 1u);
+    const uint32_t g = i >> 1;
+    c.s = (int)fast_div(g, p.div_cpr);
+    c.chunk = (int)(g - (uint32_t)c.s * p.div_cpr.d);
+    c.slot = which;
+    c.ks = 0;
+    c.is_draft = which == 1;
+    c.valid = true;
+    c.row = 0;
+    if (rows) {
+        const int ks = seq_len(p.R, c.s, p.ws);
+        const SeqState* st = ws_ptr<SeqState>(p.ws, p.L.seq) + c.s;
+        c.valid = ks >= 0 && __ldcg(&st->mode) == 1;
         c.row = c.valid ? (which ? __ldcg(&st->drow) : __ldcg(&st->trow)) : 0;
     }
     return c;

@@ -7,8 +7,10 @@
 namespace smcsd {
 
 // kModeSDRows: the SD final-token pass over the row (pair) each sequence draws from, all chunks
-// precise, rows looked up in the hand-off state the SD epilogue wrote.
-enum StreamMode { kModeSD = 0, kModeSMC = 1, kModeSMCStep = 2, kModeSDRows = 3 };
+// precise, rows looked up in the hand-off state the SD epilogue wrote. kModeSDResidual: the
+// residual pass over the (target, draft) row pairs of the sequences that draw a correction
+// token, a chunk of each row per item.
+enum StreamMode { kModeSD = 0, kModeSMC = 1, kModeSMCStep = 2, kModeSDRows = 3, kModeSDResidual = 4 };
 
 // One streaming pass over all logits rows (SD first pass, SMC reweight, fused SMC step).
 struct StreamParams {

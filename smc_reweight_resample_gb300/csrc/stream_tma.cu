@@ -154,7 +154,10 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 // slot with the block-local sequence number k = 32 * round + slot and the chunk's index. A lane out
 // of chunks tags its slot kTagDone. The lanes poll their slots together (one non-blocking test per
 // lane per pass), so no lane spins alone while the others wait on it.
-template <int DT, bool kSDRows>
+// KIND 0: the two lists of the verify and SMC passes; 1: the SD rows pass (kModeSDRows);
+// 2: the SD residual pass (kModeSDResidual), pairs of slots (2j, 2j+1) holding the target and
+// draft chunk of one pair, pairs dealt round-robin over the blocks.
+template <int DT, int KIND>
 __device__ __noinline__ void tma_producer(const StreamParams& p, unsigned char* ring,
                                           uint64_t* full, uint64_t* empty,
                                           unsigned long long* tag, unsigned* n_done, int slot,
@@ -186,7 +189,14 @@ __device__ __noinline__ void tma_producer(const StreamParams& p, unsigned char* 
         q = (k - E) / m;
         r = (k - E) % m;
     }
+    // residual pairs: block b takes pairs b, b+B, ...; local chunk k is half k & 1 of pair k >> 1
+    const uint32_t Qb = KIND == 2 && p.n_precise > (long long)bu ? (uint32_t)((p.n_precise - 1 - bu) / Bu) + 1u : 0u;
     auto local_item = [&]() -> long long {  // tag item of local chunk k, or -1
+        if (KIND == 2) {
+            const uint32_t jp = k >> 1;
+            if (jp >= Qb) return -1;
+            return (long long)((((jp * Bu + bu) << 1) | (k & 1u)) | 0x80000000u);
+        }
         uint32_t j;
         bool precise;
         if (k < E) {
@@ -229,8 +239,9 @@ __device__ __noinline__ void tma_producer(const StreamParams& p, unsigned char* 
             done = true;
             continue;
         }
-        const ChunkRef c = kSDRows ? chunk_ref_sd_rows(p, (uint32_t)it, true)
-                                   : chunk_ref_two_list(p, (uint32_t)it);
+        const ChunkRef c = KIND == 1   ? chunk_ref_sd_rows(p, (uint32_t)it, true)
+                           : KIND == 2 ? chunk_ref_sd_residual(p, (uint32_t)it, true)
+                                       : chunk_ref_two_list(p, (uint32_t)it);
         const long long off = (long long)c.chunk * kChunkBytes;
         const long long left = row_bytes - off;
         const uint32_t bytes = (uint32_t)(left < kChunkBytes ? left : kChunkBytes);
@@ -268,6 +279,111 @@ __device__ __noinline__ void tma_producer(const StreamParams& p, unsigned char* 
     if (round > 0) mbar_wait(fb, (round - 1) & 1u);
 }
 
+// A consumer warp of the SD residual pass: it claims both slots of a pair (target chunk in the
+// even slot, draft chunk in the odd one), reads the sequence's residual context while the data
+// lands, and stores the double-float sums of max(0, p - q) per lane block and per chunk (residual
+// partials of the residual draw). Lane l reads its block's pieces with an XOR swizzle (piece
+// i ^ (l & 7)), conflict-free.
+template <int DT>
+__device__ __forceinline__ void residual_consumer(const StreamParams& p, const PreciseCtx& P,
+                                                  unsigned char* ring, uint64_t* full,
+                                                  uint64_t* empty, unsigned long long* tag,
+                                                  unsigned* next, unsigned* n_done, int lane) {
+    constexpr int SUB = Geo<DT>::kSub, PERP = 16 / Geo<DT>::kBytes;
+    const SeqState* seq = ws_ptr<SeqState>(p.ws, p.L.seq);
+    for (;;) {
+        unsigned k = 0;
+        if (lane == 0) k = atomicAdd(next, 2u);
+        k = __shfl_sync(0xffffffffu, k, 0);
+        const int slot0 = (int)(k % kRing), slot1 = slot0 + 1;
+        unsigned long long seen0, seen1;
+        if (!__all_sync(0xffffffffu, tag_wait(smem_u32(&tag[slot0]), k, seen0))) {
+            if (lane == 0) raise_error(p.ws, kErrTimeout);
+            break;
+        }
+        seen0 = __shfl_sync(0xffffffffu, seen0, 0);
+        if ((uint32_t)(seen0 >> 32) == kTagDone) {
+            unsigned nd = 0;
+            if (lane == 0) nd = *reinterpret_cast<volatile unsigned*>(n_done);
+            if (__shfl_sync(0xffffffffu, nd, 0) == (unsigned)kRing) break;
+            continue;
+        }
+        // both halves of a pair come from the same round of two lanes of one producer warp
+        if (!__all_sync(0xffffffffu, tag_wait(smem_u32(&tag[slot1]), k + 1, seen1))) {
+            if (lane == 0) raise_error(p.ws, kErrTimeout);
+            break;
+        }
+        const uint32_t item = (uint32_t)seen0;  // 0xffffffff: nothing loaded
+        ChunkRef c{};
+        c.valid = false;
+        if (item != 0xffffffffu) c = chunk_ref_sd_residual(p, item, false);
+        ResidualCtx rc{};
+        if (c.valid) rc = residual_ctx(seq + c.s, P);
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full[slot0]), (k / kRing) & 1u) &&
+                                         mbar_wait(smem_u32(&full[slot1]), (k / kRing) & 1u))) {
+            if (lane == 0) raise_error(p.ws, kErrTimeout);
+            break;
+        }
+        bool wrote = false;
+        if (c.valid) {
+            const long long e0 = (long long)c.chunk * Geo<DT>::kChunk + (long long)lane * SUB;
+            unsigned char* bt = ring + (size_t)slot0 * kChunkBytes + lane * 128;
+            unsigned char* bd = ring + (size_t)slot1 * kChunkBytes + lane * 128;
+            dd acc{kBias, 0.0f};
+            if (e0 < p.R.V) {
+                if (e0 + SUB > p.R.V) {
+                    // the rows end inside this block: the lane overwrites its logits past V with
+                    // -inf (the rest of the slots holds older chunks)
+                    for (int q = 0; q < SUB; ++q)
+                        if (e0 + q >= p.R.V) {
+                            if (DT == 1) {
+                                reinterpret_cast<unsigned short*>(bt)[q] = 0xff80u;
+                                reinterpret_cast<unsigned short*>(bd)[q] = 0xff80u;
+                            } else {
+                                reinterpret_cast<uint32_t*>(bt)[q] = 0xff800000u;
+                                reinterpret_cast<uint32_t*>(bd)[q] = 0xff800000u;
+                            }
+                        }
+                    wrote = true;
+                }
+                const int sw = lane & 7;
+#pragma unroll 1
+                for (int i = 0; i < kLoads; ++i) {
+                    const uint4 vt = *reinterpret_cast<const uint4*>(bt + ((i ^ sw) << 4));
+                    const uint4 vd = *reinterpret_cast<const uint4*>(bd + ((i ^ sw) << 4));
+                    const uint32_t wt[4] = {vt.x, vt.y, vt.z, vt.w}, wd[4] = {vd.x, vd.y, vd.z, vd.w};
+#pragma unroll
+                    for (int q = 0; q < PERP; ++q) {
+                        const uint32_t xt = DT == 1 ? ((q & 1) ? (wt[q >> 1] >> 16) : (wt[q >> 1] & 0xffffu)) : wt[q];
+                        const uint32_t xd = DT == 1 ? ((q & 1) ? (wd[q >> 1] >> 16) : (wd[q >> 1] & 0xffffu)) : wd[q];
+                        acc_biased(acc, residual_weight<DT>(xt, xd, rc, P));
+                    }
+                    acc = fast_two_sum(acc.hi, acc.lo);
+                }
+            }
+            const dd sv = unbias(acc);
+            float4* tot = ws_ptr<float4>(p.ws, p.L.rtot) + (size_t)c.s * p.cpr;
+            float4* sub = ws_ptr<float4>(p.ws, p.L.rsub) + (size_t)c.s * p.cpr * kSubs;
+            sub[(size_t)c.chunk * kSubs + lane] = pack_part(sv, 0);
+            const dd total = warp_sum_dd(sv);
+            if (lane == 0) tot[c.chunk] = pack_part(total, 0);
+            // stores into a slot must be ordered before the copy engine's next write to it
+            if (wrote) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        const bool any_wrote = __any_sync(0xffffffffu, wrote);
+        __syncwarp();
+        if (lane == 0) {
+            if (any_wrote) {
+                mbar_arrive(smem_u32(&empty[slot0]));
+                mbar_arrive(smem_u32(&empty[slot1]));
+            } else {
+                mbar_arrive_relaxed(smem_u32(&empty[slot0]));
+                mbar_arrive_relaxed(smem_u32(&empty[slot1]));
+            }
+        }
+    }
+}
+
 template <int DT, int MODE>
 __global__ void __launch_bounds__(kTmaThreads, 1)
     stream_tma_kernel(const __grid_constant__ StreamParams p) {
@@ -297,7 +413,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     if (threadIdx.x == 0) griddep_launch_dependents();
     if (warp < kTmaProducers) {
         constexpr int kPer = kRing / kTmaProducers;
-        tma_producer<DT, MODE == kModeSDRows>(p, ring, full, empty, tag, n_done, warp * kPer + (lane % kPer), lane < kPer);
+        tma_producer<DT, MODE == kModeSDRows ? 1 : MODE == kModeSDResidual ? 2 : 0>(
+            p, ring, full, empty, tag, n_done, warp * kPer + (lane % kPer), lane < kPer);
         return;
     }
 
@@ -313,6 +430,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         setup_exp_table(sTab, p.sc_t, sT, p.ws, ws_ptr<uint32_t>(p.ws, p.L.tab),
                         ws_ptr<float2>(p.ws, p.L.tab + 16), p.direct, tid, nthr, 1);
         P.tab = sTab;
+    }
+    if (MODE == kModeSDResidual) {
+        residual_consumer<DT>(p, P, ring, full, empty, tag, next, n_done, lane);
+        return;
     }
     for (;;) {
         unsigned k = 0;
@@ -413,7 +534,13 @@ template <int DT, int MODE>
 static cudaError_t launch_tma_t(const StreamParams& p0, cudaStream_t st) {
     auto kern = stream_tma_kernel<DT, MODE>;
     StreamParams p = p0;
-    if (MODE == kModeSDRows) {
+    if (MODE == kModeSDResidual) {
+        // (target, draft) chunk pairs of every sequence; n_precise counts pairs
+        p.fslots = 0;
+        p.n_precise = (long long)p.R.S * p.cpr;
+        p.n_fast = 0;
+        p.div_fseq = make_fastdiv(1u);
+    } else if (MODE == kModeSDRows) {
         // two rows per sequence (the second only when its draw needs it), all precise
         p.fslots = 0;
         p.n_precise = (long long)p.R.S * 2 * p.cpr;
@@ -432,7 +559,8 @@ static cudaError_t launch_tma_t(const StreamParams& p0, cudaStream_t st) {
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     const long long cap = device_sm_count();
-    const long long want = (p.n_precise + p.n_fast + kTmaConsumers - 1) / kTmaConsumers;
+    const long long units = (MODE == kModeSDResidual ? 2 : 1) * p.n_precise + p.n_fast;
+    const long long want = (units + kTmaConsumers - 1) / kTmaConsumers;
     int grid = (int)(want < cap ? want : cap);
     if (grid < 1) grid = 1;
     kern<<<grid, kTmaThreads, kSmemBytes, st>>>(p);
@@ -442,6 +570,8 @@ static cudaError_t launch_tma_t(const StreamParams& p0, cudaStream_t st) {
 cudaError_t launch_stream_tma(const StreamParams& p, cudaStream_t st) {
     if (p.mode == kModeSDRows)
         return p.dtype == 0 ? launch_tma_t<0, kModeSDRows>(p, st) : launch_tma_t<1, kModeSDRows>(p, st);
+    if (p.mode == kModeSDResidual)
+        return p.dtype == 0 ? launch_tma_t<0, kModeSDResidual>(p, st) : launch_tma_t<1, kModeSDResidual>(p, st);
     if (p.dtype == 0) {
         if (p.mode == kModeSD) return launch_tma_t<0, kModeSD>(p, st);
         if (p.mode == kModeSMC) return launch_tma_t<0, kModeSMC>(p, st);
