@@ -34,32 +34,65 @@ UNIT = "positions/s"
 NSETS = 4
 
 
-def workload_config():
+DEFAULT_WORKLOAD = "smc_sd_step_8x16_k4_v128256_bf16"
+# name -> (kind, config); "smc": one smc_step per step, "sd": one sd_verify per step
+WORKLOADS = {
+    DEFAULT_WORKLOAD: ("smc", "SMC_LLAMA3"),
+    "smc_sd_step_4x64_k8_v151936_bf16_power": ("smc", "SMC_QWEN_POWER"),
+    "sd_verify_128_k4_v128256_bf16": ("sd", "SMC_LLAMA3"),
+    "sd_verify_16_k4_v32000_bf16": ("sd", None),
+}
+
+
+def workload_config(name: str = DEFAULT_WORKLOAD):
     from smc_reweight_resample_gb300 import synth
 
-    cfg = synth.SMC_LLAMA3
-    return cfg, {
-        "workload": "smc_sd_step_8x16_k4_v128256_bf16",
-        "G": cfg.G, "N": cfg.N, "K": cfg.K, "V": cfg.V, "temperature": cfg.temperature,
-        "alpha": cfg.alpha, "ess_threshold": cfg.ess_threshold, "ctx": cfg.ctx,
-        "page": cfg.page, "positions_per_step": cfg.S * (cfg.K + 1),
-        "l2": f"inputs larger than L2: {NSETS} rotating logit sets of "
-              f"{logit_bytes(cfg) / 1e6:.1f} MB",
+    kind, cname = WORKLOADS[name]
+    if cname is None:  # the Mistral-vocabulary SD verify: 16 sequences, K=4, V=32000
+        cfg = synth.SMCConfig("sd_mistral_16_k4_v32000", 1, 16, 4, 32000, 3.0, 1.0, 1.0, 1.0, 256)
+    else:
+        cfg = getattr(synth, cname)
+    big = NSETS * logit_bytes(cfg) > 129e6
+    config = {
+        "workload": name, "K": cfg.K, "V": cfg.V, "temperature": cfg.temperature,
+        "positions_per_step": cfg.S * (cfg.K + 1),
+        "l2": (f"inputs larger than L2: {NSETS} rotating logit sets of {logit_bytes(cfg) / 1e6:.1f} MB"
+               if big else
+               f"{NSETS} rotating logit sets of {logit_bytes(cfg) / 1e6:.1f} MB; L2 flushed (256 MB "
+               f"write) before every timed graph replay of {NSETS} calls"),
     }
+    if kind == "smc":
+        config.update({"G": cfg.G, "N": cfg.N, "alpha": cfg.alpha,
+                       "ess_threshold": cfg.ess_threshold, "ctx": cfg.ctx, "page": cfg.page})
+    else:
+        config.update({"S": cfg.S})
+    return cfg, config, kind
 
 
 def logit_bytes(cfg) -> int:
     return cfg.S * (2 * cfg.K + 1) * cfg.V * 2
 
 
-def algorithmic_bytes(cfg) -> int:
+def algorithmic_bytes(cfg, kind: str = "smc") -> int:
     """Bytes one step must move: every logit once, plus tokens, uniforms, weights and tables."""
+    if kind == "sd":  # draft tokens, uniforms, accept lengths and tokens out
+        return logit_bytes(cfg) + cfg.S * cfg.K * 4 + cfg.S * (cfg.K + 1) * 4 + cfg.S * 8
     small = (cfg.S * cfg.K * 4 + cfg.S * 4 + cfg.G * 4 + cfg.S * 4 * 2 + cfg.S * 4 + cfg.G * 8
              + 2 * cfg.S * cfg.pages_per_seq * 4 + cfg.S * cfg.pages_per_seq * 4)
     return logit_bytes(cfg) + small
 
 
-KERNELS_PER_STEP = 2  # stream pass and finishing pass (the refcount memset is a copy-engine op)
+KERNELS_PER_STEP = 2  # stream pass and finishing pass (the refcount memset is a copy-engine op);
+# groups of more than 32 particles add the stand-alone resampling and page-table kernels
+SD_KERNELS_PER_CALL = 6  # stream, epilogue, rows stream and epilogue, residual stream and draw
+KERNEL_NOTE = {
+    "smc": "one smc_step call: stream_tma_kernel, finish_kernel and the 64 KB refcount memset "
+           "(kernel shares in profiles/launches_<workload>.md); achieved = algorithmic bytes per "
+           "step / device time per step",
+    "sd": "one sd_verify call: the stream over every row, the SD epilogue, the final-token rows "
+          "and residual passes with their epilogues; achieved = algorithmic bytes per call / "
+          "device time per call",
+}
 
 
 def _source_sha256() -> str:
@@ -246,7 +279,11 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    cfg, config = workload_config()
+    cfg, config, kind = workload_config(args.workload)
+    if kind != "smc":
+        print(json.dumps({"impl": "reference", "unavailable": "the timed oracle leg covers the "
+                          "SMC workloads only"}), flush=True)
+        return 0
     budget = 120.0
     per_step = max(0.02, budget / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
@@ -286,11 +323,12 @@ def run_gpu(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    cfg, config = workload_config()
-    config["parallelism"] = f"replicas x{world} (independent prompt groups per GPU, no collective)"
+    cfg, config, kind = workload_config(args.workload)
+    unit_name = "prompt groups" if kind == "smc" else "sequences"
+    config["parallelism"] = f"replicas x{world} (independent {unit_name} per GPU, no collective)"
 
     base = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and kind == "smc":
         base = cpu_baseline(cfg, args.cpu_seconds)  # before any GPU work
 
     torch.cuda.set_device(local)
@@ -313,7 +351,12 @@ def run_gpu(args):
         ur = torch.from_numpy(synth.uniforms(rank, G, stream=101 + 2 * i)).to(dev)
         sets.append((tgt, drf, toks, ub, ur))
     torch.cuda.synchronize()
-    ws = B.Workspace(B.OP_SMC_STEP, S, K, V, dev)
+    ws = B.Workspace(B.OP_SMC_STEP if kind == "smc" else B.OP_SD_VERIFY, S, K, V, dev)
+    usd = [torch.from_numpy(synth.uniforms(rank, S * (K + 1), stream=300 + i)).to(dev)
+           for i in range(NSETS)]
+    sd_out = (torch.empty(S, dtype=torch.int32, device=dev), torch.empty(S, dtype=torch.int32, device=dev))
+    small_set = NSETS * logit_bytes(cfg) <= 129e6
+    flush = torch.empty((256 << 20) if small_set else 0, dtype=torch.uint8, device=dev)
     logw = torch.zeros(S, dtype=torch.float32, device=dev)
     tables = [torch.from_numpy(synth.initial_page_table(S, P)).to(dev),
               torch.empty(S * P, dtype=torch.int32, device=dev)]
@@ -325,6 +368,10 @@ def run_gpu(args):
 
     def step(i, stream):
         tgt, drf, toks, ub, ur = sets[i % NSETS]
+        if kind == "sd":
+            B.sd_verify(tgt, drf, toks, S, K, V, cfg.temperature, usd[i % NSETS], ws=ws,
+                        accept_len=sd_out[0], out_token=sd_out[1], stream=stream)
+            return
         B.smc_step(tgt, drf, toks, G, N, K, V, cfg.temperature, cfg.alpha, ub, logw,
                    cfg.ess_threshold, ur, table_in=tables[i % 2], pages_per_seq=P,
                    num_pages=S * P, ws=ws, table_out=tables[(i + 1) % 2], stream=stream, **outs)
@@ -357,13 +404,28 @@ def run_gpu(args):
         dist.barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
+    ms_flushed = None
     with torch.cuda.stream(stream):
-        ev0.record(stream)
-        for _ in range(reps):
-            graph.replay()
-        for i in range(tail):
-            step(i, stream)
-        ev1.record(stream)
+        if small_set:  # working set inside L2: time each graph replay after an L2 flush
+            ms_flushed = 0.0
+            for r in range(reps):
+                flush.fill_(r & 255)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                graph.replay()
+                e1.record(stream)
+                e1.synchronize()
+                ms_flushed += e0.elapsed_time(e1)
+            ev0.record(stream)
+            ev1.record(stream)
+        else:
+            ev0.record(stream)
+            for _ in range(reps):
+                graph.replay()
+            for i in range(tail):
+                step(i, stream)
+            ev1.record(stream)
     ev1.synchronize()
     torch.cuda.synchronize()
     t_wall1 = time.time()
@@ -372,6 +434,9 @@ def run_gpu(args):
     time.sleep(0.3)
     clocks.stop()
     ms = ev0.elapsed_time(ev1)
+    if ms_flushed is not None:
+        ms = ms_flushed
+        args.steps = reps * NSETS
     if world > 1:
         t = torch.tensor([ms], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -383,7 +448,7 @@ def run_gpu(args):
 
     # e2e: inputs from pinned host memory, results back to the host, every step
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and kind == "smc":
         e_steps = min(args.steps, args.e2e_steps)
         host_sets = []
         for i in range(2):
@@ -429,7 +494,7 @@ def run_gpu(args):
     if rank != 0:
         return 0
     peak, peak_kind = measured_peaks()
-    alg = algorithmic_bytes(cfg)
+    alg = algorithmic_bytes(cfg, kind)
     achieved = alg / (ms_per_step / 1000.0) / 1e9
     traffic = args.ncu_traffic if args.ncu_traffic is not None else recorded_traffic(config["workload"])
     line = {
@@ -439,14 +504,14 @@ def run_gpu(args):
         "config": config,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "one smc_step call: stream_tma_kernel, finish_kernel and the 64 KB "
-                               "refcount memset (kernel shares in profiles/launches_<workload>.md); "
-                               "achieved = algorithmic bytes per step / device time per step",
+                     "kernel": KERNEL_NOTE[kind],
                      "traffic_source": "profiles/traffic_<workload>.txt (ncu dram bytes of one step)",
                      "peak_kind": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
                      "algorithmic_bytes_per_launch": alg,
                      "frac_of_8TBps_spec": achieved / 8000.0},
-        "cpu_baseline": base, "e2e": e2e, "gpu_launches": args.steps * KERNELS_PER_STEP,
+        "cpu_baseline": base, "e2e": e2e,
+        "gpu_launches": args.steps * (SD_KERNELS_PER_CALL if kind == "sd" else
+                                      KERNELS_PER_STEP + (2 if cfg.N > 32 else 0)),
         "clocks": clocks.summary(t_wall0, t_wall1),
     }
     print(json.dumps(line), flush=True)
@@ -463,6 +528,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=40)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS),
+                    help="the default is the headline workload; the others are extra measurements")
     ap.add_argument("--ncu-traffic", type=float, default=None,
                     help="dram bytes per launch of the dominant kernel from an ncu capture")
     args = ap.parse_args(argv)
