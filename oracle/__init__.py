@@ -48,12 +48,16 @@ def _load():
             lib.oracle_sample_inverse_cdf.argtypes = [P, i, d, P, P]
             lib.oracle_sd_verify.argtypes = [P, P, i, P, P, P, i, i, i, f, P, P, P, P, P, P, P]
             lib.oracle_smc_reweight.argtypes = [P, P, i, P, i, i, i, f, f, P, P, P, P, P, P, P]
+            lib.oracle_smc_reweight_tilted.argtypes = [P, P, i, P, i, i, i, f, f, i, P, f, P, P, P,
+                                                       P, P, P, P]
             lib.oracle_ess_resample.argtypes = [P, i, i, f, P, P, P, P, P, P]
             lib.oracle_pagetable_remap.argtypes = [P, P, i, i, P, P, i, P, i]
             lib.oracle_pacer_block_stop.argtypes = [P, P, f, i, i, i, i, f, f, P, P, P]
+            lib.oracle_pacer_block_stop_pos.argtypes = [P, P, P, f, i, i, i, i, f, f, P, P, P]
             for fn in (lib.oracle_row_lse, lib.oracle_sample_inverse_cdf, lib.oracle_sd_verify,
-                       lib.oracle_smc_reweight, lib.oracle_ess_resample, lib.oracle_pagetable_remap,
-                       lib.oracle_pacer_block_stop):
+                       lib.oracle_smc_reweight, lib.oracle_smc_reweight_tilted,
+                       lib.oracle_ess_resample, lib.oracle_pagetable_remap,
+                       lib.oracle_pacer_block_stop, lib.oracle_pacer_block_stop_pos):
                 fn.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -154,6 +158,39 @@ def smc_reweight(tgt, drf, draft_tokens, S, K, V, temperature, alpha, uniforms, 
     return out
 
 
+TARGET_TOKEN, TARGET_SEQUENCE = 0, 1
+
+
+def smc_reweight_tilted(tgt, drf, draft_tokens, S, K, V, temperature, alpha, uniforms, logw,
+                        target_mode=TARGET_TOKEN, log_reward=None, reward_scale=0.0,
+                        raise_on_error=True):
+    """Reweight with the per-position (TARGET_TOKEN) or whole-sequence (TARGET_SEQUENCE) power
+    target and an optional additive log-reward; same dict as ``smc_reweight``."""
+    lib = _load()
+    tgt = np.ascontiguousarray(tgt)
+    drf = np.ascontiguousarray(drf)
+    dt = _dtype_code(tgt)
+    draft_tokens = np.ascontiguousarray(draft_tokens, dtype=np.int32)
+    uniforms = np.ascontiguousarray(uniforms, dtype=np.float32)
+    rw = None if log_reward is None else np.ascontiguousarray(log_reward, dtype=np.float32)
+    lw = np.array(logw, dtype=np.float32, copy=True)
+    out = dict(
+        logw=lw, bonus_token=np.full(S, -7, np.int32), lse_tgt=np.full(S * (K + 1), np.nan),
+        lse_drf=np.full(max(S * K, 1), np.nan), bonus_margin=np.full(S, np.nan),
+        dlogw=np.full(S, np.nan),
+    )
+    rc = lib.oracle_smc_reweight_tilted(_p(tgt), _p(drf), dt, _p(draft_tokens), S, K, V,
+                                        float(temperature), float(alpha), int(target_mode), _p(rw),
+                                        float(reward_scale), _p(uniforms), _p(lw),
+                                        _p(out["bonus_token"]), _p(out["lse_tgt"]),
+                                        _p(out["lse_drf"]), _p(out["bonus_margin"]),
+                                        _p(out["dlogw"]))
+    out["status"] = rc
+    if raise_on_error:
+        _check(rc, "smc_reweight_tilted")
+    return out
+
+
 def ess_resample(logw, G, N, ess_threshold, uniforms, raise_on_error=True):
     lib = _load()
     lw = np.array(logw, dtype=np.float32, copy=True)
@@ -187,15 +224,24 @@ def pagetable_remap(ancestors, resampled, G, N, table_in, pages_per_seq, num_pag
     return dict(table_out=tout, refcount=rc_arr, status=rc)
 
 
-def pacer_block_stop(hidden, w, c, S, b, max_blocks, d, t0, rho, raise_on_error=True):
+def pacer_block_stop(hidden, w, c, S, b, max_blocks, d, t0, rho, pos_emb=None,
+                     raise_on_error=True):
+    """``pos_emb``: optional bf16 bits [max_blocks*b, d] added to every sequence's hidden states."""
     lib = _load()
     hidden = np.ascontiguousarray(hidden, dtype=np.uint16)
     w = np.ascontiguousarray(w, dtype=np.uint16)
     out = dict(lengths=np.full(S, -7, np.int32), block_scores=np.full(S * max_blocks, np.nan),
                margin=np.full(S, np.nan))
-    rc = lib.oracle_pacer_block_stop(_p(hidden), _p(w), float(c), S, b, max_blocks, d,
-                                     float(t0), float(rho), _p(out["lengths"]),
-                                     _p(out["block_scores"]), _p(out["margin"]))
+    if pos_emb is None:
+        rc = lib.oracle_pacer_block_stop(_p(hidden), _p(w), float(c), S, b, max_blocks, d,
+                                         float(t0), float(rho), _p(out["lengths"]),
+                                         _p(out["block_scores"]), _p(out["margin"]))
+    else:
+        pe = np.ascontiguousarray(pos_emb, dtype=np.uint16)
+        assert pe.size == max_blocks * b * d
+        rc = lib.oracle_pacer_block_stop_pos(_p(hidden), _p(w), _p(pe), float(c), S, b, max_blocks,
+                                             d, float(t0), float(rho), _p(out["lengths"]),
+                                             _p(out["block_scores"]), _p(out["margin"]))
     out["status"] = rc
     if raise_on_error:
         _check(rc, "pacer_block_stop")

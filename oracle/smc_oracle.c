@@ -274,31 +274,54 @@ int oracle_sd_verify(const void* tgt, const void* drf, int dtype, const int32_t*
 
 /*
  * [SMC] sec. 2 step 3: each particle's weight is updated by the ratio of target to draft
- * probability of its K draft tokens, in log space:
- *     logw_s += sum_{k<K} ( log pi_k(x_k) - log q_k(x_k) ),
- * pi = softmax(alpha * z_t / T) (alpha = 1 is the plain target p; alpha != 1 is the
- * power target p^alpha renormalised, [SMC] sec. 3 "power sampling"), q = softmax(z_d/T).
- * [SMC] sec. 2 "exactly K+1 tokens per particle": the (K+1)-th token is drawn from pi at
- * target row K with uniforms[s]; its weight factor pi/pi is 1, so it adds nothing.
+ * probability of its K draft tokens, in log space.  [SMC] sec. 3 ("flexibility") names
+ * modified targets, power sampling and reward-weighted decoding, and sec. 5
+ * ("extensibility") reward optimisation and hard constraints through the same importance
+ * weights; two readings of a power target are offered (target_mode):
+ *
+ *  0 (per position): pi = softmax(alpha * z_t / T) at every position (alpha = 1 is the
+ *    plain target p; alpha != 1 is p^alpha renormalised per position), q = softmax(z_d/T):
+ *        logw_s += sum_{k<K} ( log pi_k(x_k) - log q_k(x_k) );
+ *    the (K+1)-th token ([SMC] sec. 2 "exactly K+1 tokens per particle") is drawn from pi
+ *    at target row K with uniforms[s]; its weight factor pi/pi is 1, so it adds nothing.
+ *
+ *  1 (whole sequence): the target is the unnormalised power of the sequence probability,
+ *    gamma(x) = prod_t p_t(x_t)^alpha with p = softmax(z_t / T).  Importance sampling of
+ *    gamma under the proposals used (q for the draft tokens, p for the (K+1)-th token)
+ *    gives
+ *        logw_s += sum_{k<K} ( alpha * log p_k(x_k) - log q_k(x_k) )
+ *                  + (alpha - 1) * log p_K(b_s),
+ *    where b_s is drawn from p at target row K with uniforms[s].  alpha = 1 gives the same
+ *    result as mode 0.
+ *
+ * In both modes, when log_reward is given, logw_s += reward_scale * log_reward[s] (an
+ * additive log-potential per particle; a NaN or infinite reward is OR_ENONFINITE).
  *
  * Layout: target rows s*(K+1)+k, draft rows s*K+k, draft_tokens[s*K+k].
  * logw is float32 in/out: the update is done in double and rounded once on store.
- * Optional outputs: lse_tgt[S*(K+1)], lse_drf[S*K], bonus_margin[S], dlogw[S] (the
- * double increment before rounding).
+ * Optional outputs: lse_tgt[S*(K+1)] (normalisers at the target's scale: alpha/T in mode 0,
+ * 1/T in mode 1), lse_drf[S*K], bonus_margin[S], dlogw[S] (the double increment before
+ * rounding).
  */
-int oracle_smc_reweight(const void* tgt, const void* drf, int dtype, const int32_t* draft_tokens,
-                        int S, int K, int V, float temperature, float alpha,
-                        const float* uniforms, float* logw, int32_t* bonus_token,
-                        double* lse_tgt, double* lse_drf, double* bonus_margin,
-                        double* dlogw) {
+int oracle_smc_reweight_tilted(const void* tgt, const void* drf, int dtype,
+                               const int32_t* draft_tokens, int S, int K, int V,
+                               float temperature, float alpha, int target_mode,
+                               const float* log_reward, float reward_scale,
+                               const float* uniforms, float* logw, int32_t* bonus_token,
+                               double* lse_tgt, double* lse_drf, double* bonus_margin,
+                               double* dlogw) {
     if (!tgt || !drf || !uniforms || !logw || !bonus_token) return OR_EINVAL;
     if (K > 0 && !draft_tokens) return OR_EINVAL;
     if (S <= 0 || K < 0 || V <= 0) return OR_EINVAL;
     if (!(temperature > 0.0f) || isinf(temperature)) return OR_EINVAL;
     if (!(alpha > 0.0f) || isinf(alpha)) return OR_EINVAL;
+    if (target_mode != 0 && target_mode != 1) return OR_EINVAL;
+    if (log_reward && (isnan(reward_scale) || isinf(reward_scale))) return OR_EINVAL;
     if (dtype != 0 && dtype != 1) return OR_EDTYPE;
-    const double scale_t = (double)alpha / (double)temperature;
+    const double a = (double)alpha;
+    const double scale_t = target_mode == 0 ? a / (double)temperature : 1.0 / (double)temperature;
     const double scale_d = 1.0 / (double)temperature;
+    const double w_t = target_mode == 0 ? 1.0 : a; /* factor on log p of a draft token */
 
     double* r = (double*)malloc(sizeof(double) * (size_t)V);
     if (!r) return OR_EINVAL;
@@ -315,14 +338,13 @@ int oracle_smc_reweight(const void* tgt, const void* drf, int dtype, const int32
             if (lse_drf) lse_drf[dr] = Ld;
             const int x = draft_tokens[dr];
             if (x < 0 || x >= V) { rc = OR_ERANGE; break; }
-            inc += row_logprob(tgt, dtype, tr, V, scale_t, Lt, x) -
-                   row_logprob(drf, dtype, dr, V, scale_d, Ld, x);
+            const double lp = row_logprob(tgt, dtype, tr, V, scale_t, Lt, x);
+            const double lq = row_logprob(drf, dtype, dr, V, scale_d, Ld, x);
+            inc += target_mode == 0 ? lp - lq : w_t * lp - lq;
         }
         if (rc != OR_OK) break;
-        if (dlogw) dlogw[s] = inc;
-        logw[s] = (float)((double)logw[s] + inc);
 
-        /* bonus token from pi at target row K */
+        /* (K+1)-th token from the target's row K at its scale */
         const long long tr = (long long)s * (K + 1) + K;
         double LK;
         rc = oracle_row_lse(tgt, dtype, tr, V, scale_t, &LK);
@@ -337,9 +359,30 @@ int oracle_smc_reweight(const void* tgt, const void* drf, int dtype, const int32
         }
         bonus_token[s] = tok;
         if (bonus_margin) bonus_margin[s] = marg;
+        if (target_mode == 1)
+            inc += (a - 1.0) * row_logprob(tgt, dtype, tr, V, scale_t, LK, tok);
+
+        if (log_reward) {
+            const double rw = (double)log_reward[s];
+            if (isnan(rw) || isinf(rw)) { rc = OR_ENONFINITE; break; }
+            inc += (double)reward_scale * rw;
+        }
+        if (dlogw) dlogw[s] = inc;
+        logw[s] = (float)((double)logw[s] + inc);
     }
     free(r);
     return rc;
+}
+
+/* The per-position target of mode 0 above, without a reward term. */
+int oracle_smc_reweight(const void* tgt, const void* drf, int dtype, const int32_t* draft_tokens,
+                        int S, int K, int V, float temperature, float alpha,
+                        const float* uniforms, float* logw, int32_t* bonus_token,
+                        double* lse_tgt, double* lse_drf, double* bonus_margin,
+                        double* dlogw) {
+    return oracle_smc_reweight_tilted(tgt, drf, dtype, draft_tokens, S, K, V, temperature, alpha,
+                                      0, NULL, 0.0f, uniforms, logw, bonus_token, lse_tgt,
+                                      lse_drf, bonus_margin, dlogw);
 }
 
 /* ------------------------------------------------------------------------------------ */
@@ -483,13 +526,20 @@ int oracle_pagetable_remap(const int32_t* ancestors, const int32_t* resampled, i
  *       m_i = (1/b) sum_{j in block i} score_j;
  *       if m_i < t: length = (i+1)*b, stop;  else t = t * rho;
  *   no stop: length = max_blocks * b.
+ * The layer reads the block's hidden states together with position embeddings
+ * (Methodik 1; the ablation in "Ergebnisse" finds them essential).  With a position
+ * embedding table e (bf16 [max_blocks*b, d], row j for draft position j of every
+ * sequence) the head's input is h_j + e_j:
+ *     score_j = 1 / (1 + exp(-(sum_d w_d (h_{j,d} + e_{j,d}) + c))),
+ * and without one (pos_emb NULL) it is h_j alone.
  * hidden: bf16 [S, max_blocks*b, d]; w: bf16 [d].  block_scores[S*max_blocks] (optional)
  * receives m_i for scored blocks and -1 for blocks after the stop; margin[S] (optional)
  * receives min_i |m_i - t_i| over the comparisons made.
  */
-int oracle_pacer_block_stop(const uint16_t* hidden, const uint16_t* w, float c, int S, int b,
-                            int max_blocks, int d, float t0, float rho, int32_t* lengths,
-                            double* block_scores, double* margin) {
+int oracle_pacer_block_stop_pos(const uint16_t* hidden, const uint16_t* w,
+                                const uint16_t* pos_emb, float c, int S, int b, int max_blocks,
+                                int d, float t0, float rho, int32_t* lengths,
+                                double* block_scores, double* margin) {
     if (!hidden || !w || !lengths || S <= 0 || b <= 0 || max_blocks <= 0 || d <= 0)
         return OR_EINVAL;
     if (isnan(c) || isinf(c) || isnan(t0) || isinf(t0) || !(rho > 0.0f) || isinf(rho))
@@ -508,9 +558,14 @@ int oracle_pacer_block_stop(const uint16_t* hidden, const uint16_t* w, float c, 
             double msum = 0.0;
             for (int j = i * b; j < (i + 1) * b; ++j) {
                 const uint16_t* h = hidden + ((long long)s * P + j) * d;
+                const uint16_t* e = pos_emb ? pos_emb + (long long)j * d : NULL;
                 double dot = 0.0;
-                for (int k = 0; k < d; ++k)
-                    dot += bf16_bits_to_double(w[k]) * bf16_bits_to_double(h[k]);
+                for (int k = 0; k < d; ++k) {
+                    /* h + e of two bf16 values is exact in double */
+                    const double x = e ? bf16_bits_to_double(h[k]) + bf16_bits_to_double(e[k])
+                                       : bf16_bits_to_double(h[k]);
+                    dot += bf16_bits_to_double(w[k]) * x;
+                }
                 double a = dot + (double)c;
                 if (isnan(a)) return OR_ENONFINITE;
                 msum += 1.0 / (1.0 + exp(-a));
@@ -530,4 +585,12 @@ int oracle_pacer_block_stop(const uint16_t* hidden, const uint16_t* w, float c, 
         if (margin) margin[s] = mm;
     }
     return OR_OK;
+}
+
+/* The stop rule above without position embeddings. */
+int oracle_pacer_block_stop(const uint16_t* hidden, const uint16_t* w, float c, int S, int b,
+                            int max_blocks, int d, float t0, float rho, int32_t* lengths,
+                            double* block_scores, double* margin) {
+    return oracle_pacer_block_stop_pos(hidden, w, NULL, c, S, b, max_blocks, d, t0, rho, lengths,
+                                       block_scores, margin);
 }

@@ -15,7 +15,9 @@ arithmetic of the method itself: it only draws random numbers and lays them out.
 * Draft tokens: each draft token is drawn from its own draft row at temperature T by the
   Gumbel-max trick (argmax of z/T plus Gumbel noise). This stands in for the draft model's
   sampler, which precedes the verify step and is not part of it.
-* Hidden states for the stop rule: N(0,1) rounded to bf16; head weights N(0, 1/d).
+* Hidden states for the stop rule: N(0,1) rounded to bf16; head weights N(0, 1/d); position
+  embeddings N(0,1) rounded to bf16.
+* Log-rewards of a reward-tilted target: N(0,1) float32 per particle.
 
 The logit distributions and vocabulary sizes follow the synthetic workloads stated for
 the path (Mistral-size V=32000, Llama-3 V=128256, Qwen2.5 V=151936, DeepSeek-Coder
@@ -223,6 +225,19 @@ def pacer_case(seed: int = 0, S: int = 64, b: int = 4, max_blocks: int = 5, d: i
     h = bf16_bits(rng.normal(0.0, 1.0, (S, max_blocks * b, d)).astype(np.float32))
     w = bf16_bits(rng.normal(0.0, 1.0 / np.sqrt(d), d).astype(np.float32))
     return PacerCase(S, b, max_blocks, d, c, t0, rho, h, w)
+
+
+def pacer_pos_emb(seed: int, max_blocks: int, b: int, d: int, sigma: float = 1.0) -> np.ndarray:
+    """Position embeddings for the stop rule's head: N(0, sigma) bf16 [max_blocks*b, d], one
+    row per draft position, shared by all sequences."""
+    rng = _rng(seed, 37)
+    return bf16_bits(rng.normal(0.0, sigma, (max_blocks * b, d)).astype(np.float32))
+
+
+def log_rewards(seed: int, S: int, sigma: float = 1.0) -> np.ndarray:
+    """Per-particle log-rewards for a reward-tilted target: N(0, sigma) float32 [S]."""
+    rng = _rng(seed, 41)
+    return rng.normal(0.0, sigma, S).astype(np.float32)
 
 
 def ragged_sd_case(seed: int, lengths: np.ndarray, V: int, sigma_d: float = 3.0,

@@ -4,7 +4,10 @@ against a threshold that grows by rho after each block that passes; the block th
 is kept.
 
 Pins: a hand-derived example (tests/golden/pacer_hand.json), closed forms with a zero
-head (every score is sigmoid(c)), the length range, and monotonicity in t0.
+head (every score is sigmoid(c)), the length range, and monotonicity in t0. With position
+embeddings (Methodik 1): a hand-derived example (tests/golden/pacer_pos_hand.json), zero
+embeddings give the plain rule, and on inputs whose sums h + e are exact the rule equals
+the plain rule on the summed states.
 """
 import json
 import math
@@ -85,3 +88,48 @@ def test_scores_match_library_sigmoid(orc):
     m = expit(h @ w + 0.25).reshape(cs.S, cs.max_blocks, cs.b).mean(-1)
     np.testing.assert_allclose(out["block_scores"].reshape(cs.S, -1), m, atol=1e-12)
     assert (out["lengths"] == cs.b * cs.max_blocks).all()
+
+
+# -------------------------------------------------------------------------------------------
+# position embeddings (Methodik 1: hidden states together with position embeddings)
+# -------------------------------------------------------------------------------------------
+
+
+def test_pos_emb_hand_worked_example(orc):
+    with open(os.path.join(GOLDEN, "pacer_pos_hand.json")) as f:
+        g = json.load(f)
+    h = synth.bf16_bits(np.array(g["hidden"], np.float32))
+    w = synth.bf16_bits(np.array(g["w"], np.float32))
+    e = synth.bf16_bits(np.array(g["pos_emb"], np.float32))
+    out = orc.pacer_block_stop(h, w, g["c"], 2, g["b"], g["max_blocks"], g["d"], g["t0"], g["rho"],
+                               pos_emb=e)
+    np.testing.assert_array_equal(out["lengths"], g["lengths"])
+    np.testing.assert_allclose(out["block_scores"], np.ravel(g["block_scores"]), atol=1e-12)
+
+
+def test_zero_pos_emb_is_the_plain_rule(orc):
+    cs = synth.pacer_case(3, S=8, d=128)
+    e = np.zeros((cs.max_blocks * cs.b, cs.d), np.uint16)
+    a = orc.pacer_block_stop(cs.hidden, cs.w, 0.1, cs.S, cs.b, cs.max_blocks, cs.d, 0.5, 1.1)
+    b = orc.pacer_block_stop(cs.hidden, cs.w, 0.1, cs.S, cs.b, cs.max_blocks, cs.d, 0.5, 1.1,
+                             pos_emb=e)
+    for k in ("lengths", "block_scores", "margin"):
+        np.testing.assert_array_equal(a[k], b[k])
+
+
+def test_pos_emb_equals_plain_rule_on_summed_states(orc):
+    """h and e on a grid of eighths in [-1/2, 1/2], so that every h + e is exact in bf16: the rule
+    with embeddings equals the plain rule on hidden states h + e, position by position."""
+    S, b, nb, d = 6, 4, 5, 32
+    rng = np.random.default_rng(7)
+    hf = rng.integers(-4, 5, (S, nb * b, d)).astype(np.float32) / 8
+    ef = rng.integers(-4, 5, (nb * b, d)).astype(np.float32) / 8
+    w = synth.bf16_bits(rng.normal(0, 0.5, d).astype(np.float32))
+    a = orc.pacer_block_stop(synth.bf16_bits(hf), w, 0.05, S, b, nb, d, 0.45, 1.1,
+                             pos_emb=synth.bf16_bits(ef))
+    summed = synth.bf16_bits(hf + ef[None])
+    assert np.array_equal(synth.bf16_widen(summed), hf + ef[None])  # the sums are exact
+    p = orc.pacer_block_stop(summed, w, 0.05, S, b, nb, d, 0.45, 1.1)
+    for k in ("lengths", "block_scores"):
+        np.testing.assert_array_equal(a[k], p[k])
+    assert len(set(a["lengths"].tolist())) > 1  # the case exercises several stop points
