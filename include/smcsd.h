@@ -65,6 +65,10 @@ extern "C" {
 #define SMCSD_F32 0
 #define SMCSD_BF16 1
 
+/* targets of the tilted SMC reweight (smc_reweight_tilted, smc_step_tilted) */
+#define SMCSD_TARGET_TOKEN 0    /* per position: pi = softmax(alpha z / T), as smc_reweight */
+#define SMCSD_TARGET_SEQUENCE 1 /* whole sequence: prod_t p_t(x_t)^alpha, p = softmax(z / T) */
+
 /* operation ids for smcsd_workspace_size */
 #define SMCSD_OP_SD_VERIFY 0
 #define SMCSD_OP_SMC_REWEIGHT 1
@@ -132,6 +136,27 @@ int smc_reweight(const void* tgt_logits, const void* drf_logits, int dtype,
                  float* lse_tgt, float* lse_drf, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * SMC-SD reweight toward a tilted target ([SMC] sec. 3 "flexibility": modified targets such as
+ * power sampling and reward-weighted decoding; sec. 5: reward optimisation and hard
+ * constraints through the same importance weights). Arguments and layout as smc_reweight, plus:
+ *   target = SMCSD_TARGET_TOKEN: smc_reweight's per-position target pi = softmax(alpha z_t / T).
+ *   target = SMCSD_TARGET_SEQUENCE: the unnormalised power of the sequence probability,
+ *     prod_t p_t(x_t)^alpha with p = softmax(z_t / T). The draft tokens are proposed by q and
+ *     the (K+1)-th token b_s is drawn from p at target row K (with uniforms[s]), so
+ *       logw[s] += sum_{k<K} ( alpha log p_k(x_k) - log q_k(x_k) ) + (alpha - 1) log p_K(b_s).
+ *     alpha = 1 gives smc_reweight's result. lse_tgt then holds the normalisers at 1/T.
+ *   log_reward: optional float [S] (NULL for none); logw[s] += reward_scale * log_reward[s].
+ *     A NaN or infinite reward is SMCSD_ERR_NONFINITE (device side, smcsd_check_status);
+ *     reward_scale must be finite when log_reward is given.
+ * target other than the two values above: SMCSD_ERR_INVALID_ARG.
+ */
+int smc_reweight_tilted(const void* tgt_logits, const void* drf_logits, int dtype,
+                        const int32_t* draft_tokens, int S, int K, int V, float temperature,
+                        float alpha, int target, const float* log_reward, float reward_scale,
+                        const float* uniforms, float* logw, int32_t* bonus_token,
+                        float* lse_tgt, float* lse_drf, void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Effective sample size and systematic resampling per group of N particles ([SMC] sec. 2
  * step 4; the textbook forms, in double precision):
  *   w_i = exp(logw_i - max logw), ess[g] = (sum w)^2 / sum w^2;
@@ -158,6 +183,19 @@ int smc_ess_resample(float* logw, int G, int N, float ess_threshold, const float
 int kv_pagetable_remap(const int32_t* ancestors, const int32_t* resampled, int G, int N,
                        const int32_t* table_in, int32_t* table_out, int pages_per_seq,
                        int32_t* refcount, int num_pages, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * pacer_block_stop with position embeddings ([PACER] Methodik 1: the pre-verification layer
+ * reads the block's hidden states together with position embeddings; the ablation under
+ * "Ergebnisse" finds them essential). pos_emb: bf16 [max_blocks*b, d], row j for draft position
+ * j, shared by all sequences (NULL: pacer_block_stop). The score of position j is
+ *   score_j = sigmoid(w . (h_j + pos_emb_j) + c);
+ * everything else is as in pacer_block_stop below.
+ */
+int pacer_block_stop_pos(const void* hidden, const void* w, const void* pos_emb, float c, int S,
+                         int b, int max_blocks, int d, float t0, float rho, int32_t* lengths,
+                         float* block_scores, int32_t* tgt_offsets, int32_t* drf_offsets,
+                         void* ws, size_t ws_bytes, void* stream);
 
 /*
  * PACER blockwise stop ([PACER] Methodik 1-3), with the pre-verification layer modelled as
@@ -190,6 +228,20 @@ int smc_step(const void* tgt_logits, const void* drf_logits, int dtype,
              float* ess, int32_t* resampled, const int32_t* table_in, int32_t* table_out,
              int pages_per_seq, int32_t* refcount, int num_pages,
              void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * smc_step toward a tilted target: target, log_reward and reward_scale as in
+ * smc_reweight_tilted; everything else as in smc_step. The reward enters the log-weights
+ * before the group's ESS and resampling.
+ */
+int smc_step_tilted(const void* tgt_logits, const void* drf_logits, int dtype,
+                    const int32_t* draft_tokens, int G, int N, int K, int V, float temperature,
+                    float alpha, int target, const float* log_reward, float reward_scale,
+                    const float* bonus_uniforms, float* logw, int32_t* bonus_token,
+                    float ess_threshold, const float* resample_uniforms, int32_t* ancestors,
+                    float* ess, int32_t* resampled, const int32_t* table_in, int32_t* table_out,
+                    int pages_per_seq, int32_t* refcount, int num_pages,
+                    void* ws, size_t ws_bytes, void* stream);
 
 /*
  * smc_step without a workspace argument. None of the pages has a counterpart: this is an

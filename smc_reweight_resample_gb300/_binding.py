@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(_HERE, "libsmcsd.so")
 
 OK, ERR_INVALID_ARG, ERR_DTYPE, ERR_WORKSPACE, ERR_CUDA, ERR_NONFINITE, ERR_RANGE, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5, -6, -7
 F32, BF16 = 0, 1
+TARGET_TOKEN, TARGET_SEQUENCE = 0, 1
 OP_SD_VERIFY, OP_SMC_REWEIGHT, OP_SMC_STEP, OP_ESS_RESAMPLE, OP_PAGETABLE_REMAP, OP_PACER_BLOCK_STOP = range(6)
 
 _lib = None
@@ -53,9 +54,14 @@ def load(path: str = LIB_PATH):
                              P, sz, P]
     lib.smc_step_static.argtypes = [P, P, i, P, i, i, i, i, f, f, P, P, P, f, P, P, P, P, P, P, i,
                                     P, i, P, P]
+    lib.smc_reweight_tilted.argtypes = [P, P, i, P, i, i, i, f, f, i, P, f, P, P, P, P, P, P, sz, P]
+    lib.smc_step_tilted.argtypes = [P, P, i, P, i, i, i, i, f, f, i, P, f, P, P, P, f, P, P, P, P,
+                                    P, P, i, P, i, P, sz, P]
+    lib.pacer_block_stop_pos.argtypes = [P, P, P, f, i, i, i, i, f, f, P, P, P, P, P, sz, P]
     for fn in ("smcsd_workspace_init", "smcsd_check_status", "sd_verify", "smc_reweight",
                "smc_ess_resample", "kv_pagetable_remap", "pacer_block_stop", "smc_step",
-               "smc_step_static"):
+               "smc_step_static", "smc_reweight_tilted", "smc_step_tilted",
+               "pacer_block_stop_pos"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -155,6 +161,26 @@ def smc_reweight(tgt_logits, drf_logits, draft_tokens, S, K, V, temperature, alp
     return bonus_token
 
 
+def smc_reweight_tilted(tgt_logits, drf_logits, draft_tokens, S, K, V, temperature, alpha,
+                        uniforms, logw, target=TARGET_SEQUENCE, log_reward=None,
+                        reward_scale=0.0, ws=None, bonus_token=None, lse_tgt=None, lse_drf=None,
+                        stream=None):
+    """smc_reweight toward the per-position (TARGET_TOKEN) or whole-sequence (TARGET_SEQUENCE)
+    power target, with an optional additive log-reward float32 [S]. Updates logw in place;
+    returns bonus_token int32 [S]."""
+    dev = tgt_logits.device
+    ws = ws or Workspace(OP_SMC_REWEIGHT, S, K, V, dev)
+    bonus_token = _out(bonus_token, (S,), torch.int32, dev)
+    w, n = ws.args
+    rc = load().smc_reweight_tilted(_ptr(tgt_logits), _ptr(drf_logits), _dtype_code(tgt_logits),
+                                    _ptr(draft_tokens), S, K, V, float(temperature), float(alpha),
+                                    int(target), _ptr(log_reward), float(reward_scale),
+                                    _ptr(uniforms), _ptr(logw), _ptr(bonus_token), _ptr(lse_tgt),
+                                    _ptr(lse_drf), w, n, _stream(stream))
+    _check(rc, "smc_reweight_tilted")
+    return bonus_token
+
+
 def smc_ess_resample(logw, G, N, ess_threshold, uniforms, ws=None, ancestors=None, ess=None,
                      resampled=None, stream=None):
     """Updates logw in place; returns (ancestors [G*N], ess [G], resampled [G])."""
@@ -190,6 +216,13 @@ def pacer_block_stop(hidden, w, c, S, b, max_blocks, d, t0, rho, ws=None, length
                      block_scores=None, offsets=True, stream=None):
     """hidden bf16 [S, max_blocks*b, d], w bf16 [d]. Returns (lengths, block_scores,
     tgt_offsets, drf_offsets); the offsets are None when offsets=False."""
+    return pacer_block_stop_pos(hidden, w, None, c, S, b, max_blocks, d, t0, rho, ws, lengths,
+                                block_scores, offsets, stream)
+
+
+def pacer_block_stop_pos(hidden, w, pos_emb, c, S, b, max_blocks, d, t0, rho, ws=None,
+                         lengths=None, block_scores=None, offsets=True, stream=None):
+    """pacer_block_stop with position embeddings pos_emb bf16 [max_blocks*b, d] (None: none)."""
     dev = hidden.device
     ws = ws or Workspace(OP_PACER_BLOCK_STOP, S, 0, 1, dev)
     lengths = _out(lengths, (S,), torch.int32, dev)
@@ -197,11 +230,59 @@ def pacer_block_stop(hidden, w, c, S, b, max_blocks, d, t0, rho, ws=None, length
     to = torch.empty(S + 1, dtype=torch.int32, device=dev) if offsets else None
     do = torch.empty(S + 1, dtype=torch.int32, device=dev) if offsets else None
     wp, n = ws.args
-    rc = load().pacer_block_stop(_ptr(hidden), _ptr(w), float(c), S, b, max_blocks, d, float(t0),
-                                 float(rho), _ptr(lengths), _ptr(block_scores), _ptr(to), _ptr(do),
-                                 wp, n, _stream(stream))
+    if pos_emb is None:
+        rc = load().pacer_block_stop(_ptr(hidden), _ptr(w), float(c), S, b, max_blocks, d,
+                                     float(t0), float(rho), _ptr(lengths), _ptr(block_scores),
+                                     _ptr(to), _ptr(do), wp, n, _stream(stream))
+    else:
+        rc = load().pacer_block_stop_pos(_ptr(hidden), _ptr(w), _ptr(pos_emb), float(c), S, b,
+                                         max_blocks, d, float(t0), float(rho), _ptr(lengths),
+                                         _ptr(block_scores), _ptr(to), _ptr(do), wp, n,
+                                         _stream(stream))
     _check(rc, "pacer_block_stop")
     return lengths, block_scores, to, do
+
+
+def _step_outputs(dev, G, N, table_in, num_pages, bonus_token, ancestors, ess, resampled,
+                  table_out, refcount, with_refcount):
+    S = G * N
+    bonus_token = _out(bonus_token, (S,), torch.int32, dev)
+    ancestors = _out(ancestors, (S,), torch.int32, dev)
+    ess = _out(ess, (G,), torch.float32, dev)
+    resampled = _out(resampled, (G,), torch.int32, dev)
+    if table_in is not None:
+        table_out = _out(table_out, table_in.shape, torch.int32, dev)
+        if with_refcount and refcount is None:
+            refcount = torch.empty(num_pages, dtype=torch.int32, device=dev)
+    else:
+        table_out = refcount = None
+    return dict(bonus_token=bonus_token, ancestors=ancestors, ess=ess, resampled=resampled,
+                table_out=table_out, refcount=refcount)
+
+
+def smc_step_tilted(tgt_logits, drf_logits, draft_tokens, G, N, K, V, temperature, alpha,
+                    bonus_uniforms, logw, ess_threshold, resample_uniforms, target=TARGET_SEQUENCE,
+                    log_reward=None, reward_scale=0.0, table_in=None, pages_per_seq=0,
+                    num_pages=0, ws=None, bonus_token=None, ancestors=None, ess=None,
+                    resampled=None, table_out=None, refcount=None, with_refcount=True,
+                    stream=None):
+    """smc_step toward a tilted target (see smc_reweight_tilted). Updates logw in place.
+    Returns a dict of output tensors."""
+    dev = tgt_logits.device
+    ws = ws or Workspace(OP_SMC_STEP, G * N, K, V, dev)
+    o = _step_outputs(dev, G, N, table_in, num_pages, bonus_token, ancestors, ess, resampled,
+                      table_out, refcount, with_refcount)
+    w, n = ws.args
+    rc = load().smc_step_tilted(_ptr(tgt_logits), _ptr(drf_logits), _dtype_code(tgt_logits),
+                                _ptr(draft_tokens), G, N, K, V, float(temperature), float(alpha),
+                                int(target), _ptr(log_reward), float(reward_scale),
+                                _ptr(bonus_uniforms), _ptr(logw), _ptr(o["bonus_token"]),
+                                float(ess_threshold), _ptr(resample_uniforms),
+                                _ptr(o["ancestors"]), _ptr(o["ess"]), _ptr(o["resampled"]),
+                                _ptr(table_in), _ptr(o["table_out"]), pages_per_seq,
+                                _ptr(o["refcount"]), num_pages, w, n, _stream(stream))
+    _check(rc, "smc_step_tilted")
+    return o
 
 
 def smc_step(tgt_logits, drf_logits, draft_tokens, G, N, K, V, temperature, alpha,

@@ -143,12 +143,15 @@ extern "C" int sd_verify(const void* tgt_logits, const void* drf_logits, int dty
 
 static int smc_common(const void* tgt_logits, const void* drf_logits, int dtype,
                       const int32_t* draft_tokens, int S, int K, int V, float temperature,
-                      float alpha, const float* uniforms, float* logw, int32_t* bonus_token,
+                      float alpha, int target, const float* log_reward, float reward_scale,
+                      const float* uniforms, float* logw, int32_t* bonus_token,
                       void* ws, size_t ws_bytes, StreamParams& p) {
     if (dtype != SMCSD_F32 && dtype != SMCSD_BF16) return SMCSD_ERR_DTYPE;
     if (!tgt_logits || !uniforms || !logw || !bonus_token) return SMCSD_ERR_INVALID_ARG;
     if (S <= 0 || K < 0 || V <= 0) return SMCSD_ERR_INVALID_ARG;
     if (!finite_pos(temperature) || !finite_pos(alpha)) return SMCSD_ERR_INVALID_ARG;
+    if (target != SMCSD_TARGET_TOKEN && target != SMCSD_TARGET_SEQUENCE) return SMCSD_ERR_INVALID_ARG;
+    if (log_reward && !isfinite(reward_scale)) return SMCSD_ERR_INVALID_ARG;
     if (K > 0 && (!drf_logits || !draft_tokens)) return SMCSD_ERR_INVALID_ARG;
     const WsLayout L = ws_layout(S, K, V);
     int rc = check_ws(ws, ws_bytes, L.total);
@@ -157,7 +160,13 @@ static int smc_common(const void* tgt_logits, const void* drf_logits, int dtype,
     p.dtype = dtype;
     p.vec = aligned16(tgt_logits) && (K == 0 || aligned16(drf_logits)) &&
             ((size_t)V * elem_bytes(dtype)) % 16 == 0;
-    p.sc_t = make_scale((double)alpha / (double)temperature);
+    // per-position target: pi = softmax(alpha z / T); whole sequence: p = softmax(z / T), with
+    // alpha applied to the log-probabilities in the weight
+    p.target_seq = target == SMCSD_TARGET_SEQUENCE;
+    p.alpha = alpha;
+    p.log_reward = log_reward;
+    p.reward_scale = reward_scale;
+    p.sc_t = make_scale((p.target_seq ? 1.0 : (double)alpha) / (double)temperature);
     p.sc_d = make_scale(1.0 / (double)temperature);
     p.use_table = dtype == SMCSD_BF16 && p.sc_t.c <= kTabMaxScale;
     p.direct = p.use_table && p.sc_t.c <= kDirectMaxScale;
@@ -177,14 +186,17 @@ static int smc_common(const void* tgt_logits, const void* drf_logits, int dtype,
     return SMCSD_OK;
 }
 
-extern "C" int smc_reweight(const void* tgt_logits, const void* drf_logits, int dtype,
-                            const int32_t* draft_tokens, int S, int K, int V, float temperature,
-                            float alpha, const float* uniforms, float* logw, int32_t* bonus_token,
-                            float* lse_tgt, float* lse_drf, void* ws, size_t ws_bytes,
-                            void* stream) {
+extern "C" int smc_reweight_tilted(const void* tgt_logits, const void* drf_logits, int dtype,
+                                   const int32_t* draft_tokens, int S, int K, int V,
+                                   float temperature, float alpha, int target,
+                                   const float* log_reward, float reward_scale,
+                                   const float* uniforms, float* logw, int32_t* bonus_token,
+                                   float* lse_tgt, float* lse_drf, void* ws, size_t ws_bytes,
+                                   void* stream) {
     StreamParams p{};
     int rc = smc_common(tgt_logits, drf_logits, dtype, draft_tokens, S, K, V, temperature, alpha,
-                        uniforms, logw, bonus_token, ws, ws_bytes, p);
+                        target, log_reward, reward_scale, uniforms, logw, bonus_token, ws,
+                        ws_bytes, p);
     if (rc) return rc;
     p.mode = kModeSMC;
     p.lse_tgt = lse_tgt;
@@ -192,14 +204,26 @@ extern "C" int smc_reweight(const void* tgt_logits, const void* drf_logits, int 
     return from_cuda(launch_stream(p, (cudaStream_t)stream));
 }
 
-extern "C" int smc_step(const void* tgt_logits, const void* drf_logits, int dtype,
-                        const int32_t* draft_tokens, int G, int N, int K, int V,
-                        float temperature, float alpha, const float* bonus_uniforms, float* logw,
-                        int32_t* bonus_token, float ess_threshold, const float* resample_uniforms,
-                        int32_t* ancestors, float* ess, int32_t* resampled,
-                        const int32_t* table_in, int32_t* table_out, int pages_per_seq,
-                        int32_t* refcount, int num_pages, void* ws, size_t ws_bytes,
-                        void* stream) {
+extern "C" int smc_reweight(const void* tgt_logits, const void* drf_logits, int dtype,
+                            const int32_t* draft_tokens, int S, int K, int V, float temperature,
+                            float alpha, const float* uniforms, float* logw, int32_t* bonus_token,
+                            float* lse_tgt, float* lse_drf, void* ws, size_t ws_bytes,
+                            void* stream) {
+    return smc_reweight_tilted(tgt_logits, drf_logits, dtype, draft_tokens, S, K, V, temperature,
+                               alpha, SMCSD_TARGET_TOKEN, nullptr, 0.0f, uniforms, logw,
+                               bonus_token, lse_tgt, lse_drf, ws, ws_bytes, stream);
+}
+
+extern "C" int smc_step_tilted(const void* tgt_logits, const void* drf_logits, int dtype,
+                               const int32_t* draft_tokens, int G, int N, int K, int V,
+                               float temperature, float alpha, int target,
+                               const float* log_reward, float reward_scale,
+                               const float* bonus_uniforms, float* logw, int32_t* bonus_token,
+                               float ess_threshold, const float* resample_uniforms,
+                               int32_t* ancestors, float* ess, int32_t* resampled,
+                               const int32_t* table_in, int32_t* table_out, int pages_per_seq,
+                               int32_t* refcount, int num_pages, void* ws, size_t ws_bytes,
+                               void* stream) {
     if (G <= 0 || N <= 0 || (long long)G * N > 0x7fffffffLL) return SMCSD_ERR_INVALID_ARG;
     if (!resample_uniforms || !ancestors || isnan(ess_threshold)) return SMCSD_ERR_INVALID_ARG;
     const bool remap = table_in != nullptr;
@@ -211,7 +235,8 @@ extern "C" int smc_step(const void* tgt_logits, const void* drf_logits, int dtyp
     }
     StreamParams p{};
     int rc = smc_common(tgt_logits, drf_logits, dtype, draft_tokens, G * N, K, V, temperature,
-                        alpha, bonus_uniforms, logw, bonus_token, ws, ws_bytes, p);
+                        alpha, target, log_reward, reward_scale, bonus_uniforms, logw,
+                        bonus_token, ws, ws_bytes, p);
     if (rc) return rc;
     cudaStream_t st = (cudaStream_t)stream;
     p.mode = kModeSMCStep;
@@ -230,6 +255,21 @@ extern "C" int smc_step(const void* tgt_logits, const void* drf_logits, int dtyp
     if (p.refcount && cudaMemsetAsync(refcount, 0, (size_t)num_pages * sizeof(int32_t), st) != cudaSuccess)
         return SMCSD_ERR_CUDA;
     return from_cuda(launch_stream(p, st));
+}
+
+extern "C" int smc_step(const void* tgt_logits, const void* drf_logits, int dtype,
+                        const int32_t* draft_tokens, int G, int N, int K, int V,
+                        float temperature, float alpha, const float* bonus_uniforms, float* logw,
+                        int32_t* bonus_token, float ess_threshold, const float* resample_uniforms,
+                        int32_t* ancestors, float* ess, int32_t* resampled,
+                        const int32_t* table_in, int32_t* table_out, int pages_per_seq,
+                        int32_t* refcount, int num_pages, void* ws, size_t ws_bytes,
+                        void* stream) {
+    return smc_step_tilted(tgt_logits, drf_logits, dtype, draft_tokens, G, N, K, V, temperature,
+                           alpha, SMCSD_TARGET_TOKEN, nullptr, 0.0f, bonus_uniforms, logw,
+                           bonus_token, ess_threshold, resample_uniforms, ancestors, ess,
+                           resampled, table_in, table_out, pages_per_seq, refcount, num_pages,
+                           ws, ws_bytes, stream);
 }
 
 extern "C" int smc_ess_resample(float* logw, int G, int N, float ess_threshold,
@@ -259,10 +299,11 @@ extern "C" int kv_pagetable_remap(const int32_t* ancestors, const int32_t* resam
     return from_cuda(launch_remap(p, st));
 }
 
-extern "C" int pacer_block_stop(const void* hidden, const void* w, float c, int S, int b,
-                                int max_blocks, int d, float t0, float rho, int32_t* lengths,
-                                float* block_scores, int32_t* tgt_offsets, int32_t* drf_offsets,
-                                void* ws, size_t ws_bytes, void* stream) {
+extern "C" int pacer_block_stop_pos(const void* hidden, const void* w, const void* pos_emb,
+                                    float c, int S, int b, int max_blocks, int d, float t0,
+                                    float rho, int32_t* lengths, float* block_scores,
+                                    int32_t* tgt_offsets, int32_t* drf_offsets, void* ws,
+                                    size_t ws_bytes, void* stream) {
     if (!hidden || !w || !lengths) return SMCSD_ERR_INVALID_ARG;
     if (S <= 0 || b <= 0 || b > 64 || max_blocks <= 0 || d <= 0) return SMCSD_ERR_INVALID_ARG;
     if (!isfinite(c) || !isfinite(t0) || !finite_pos(rho)) return SMCSD_ERR_INVALID_ARG;
@@ -272,6 +313,7 @@ extern "C" int pacer_block_stop(const void* hidden, const void* w, float c, int 
     PacerParams p{};
     p.hidden = static_cast<const uint16_t*>(hidden);
     p.w = static_cast<const uint16_t*>(w);
+    p.pos_emb = static_cast<const uint16_t*>(pos_emb);
     p.c = c;
     p.S = S;
     p.b = b;
@@ -279,7 +321,7 @@ extern "C" int pacer_block_stop(const void* hidden, const void* w, float c, int 
     p.d = d;
     p.t0 = t0;
     p.rho = rho;
-    p.vec = aligned16(hidden) && aligned16(w) && (d % 8) == 0;
+    p.vec = aligned16(hidden) && aligned16(w) && (!pos_emb || aligned16(pos_emb)) && (d % 8) == 0;
     p.lengths = lengths;
     p.block_scores = block_scores;
     p.tgt_offsets = tgt_offsets;
@@ -287,4 +329,12 @@ extern "C" int pacer_block_stop(const void* hidden, const void* w, float c, int 
     p.ws = ws;
     p.L = ws_layout(S, 0, 1);
     return from_cuda(launch_pacer(p, (cudaStream_t)stream));
+}
+
+extern "C" int pacer_block_stop(const void* hidden, const void* w, float c, int S, int b,
+                                int max_blocks, int d, float t0, float rho, int32_t* lengths,
+                                float* block_scores, int32_t* tgt_offsets, int32_t* drf_offsets,
+                                void* ws, size_t ws_bytes, void* stream) {
+    return pacer_block_stop_pos(hidden, w, nullptr, c, S, b, max_blocks, d, t0, rho, lengths,
+                                block_scores, tgt_offsets, drf_offsets, ws, ws_bytes, stream);
 }

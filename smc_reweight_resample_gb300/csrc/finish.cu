@@ -88,7 +88,8 @@ __global__ void __launch_bounds__(kFinishMaxWarps * kWarp)
     // The sequence (and group) epilogue needs only the rows with a draft token. When the block has
     // a warp per row, the bonus row's warp (warp 2ks) keeps drawing while the others go on, meeting
     // at a named barrier without it; otherwise the whole block meets.
-    const bool split = MODE != kModeSD && nw == 2 * ks + 1 && ks > 0;
+    // (The whole-sequence power target needs the bonus row's weight factor: no split then.)
+    const bool split = MODE != kModeSD && nw == 2 * ks + 1 && ks > 0 && !p.target_seq;
     if (split && warp == 2 * ks) return;
     const int bar = split ? 1 : 0, nthr = split ? 2 * ks * kWarp : (int)blockDim.x;
     bar_sync(bar, nthr);

@@ -5,8 +5,8 @@
 //     the page reference counts rebuilt (same page, sec. 3: a metadata update, no KV movement);
 //   pacer_kernel: the PACER blockwise stop rule ("PACER: Blockwise Pre-verification for
 //     Speculative Decoding with Adaptive Length", Methodik 1-3), one block per sequence, reading
-//     hidden states only up to the block that stops; the last block to finish writes the ragged
-//     row offsets for the verify that follows.
+//     hidden states (and position embeddings, Methodik 1) only up to the block that stops; the
+//     last block to finish writes the ragged row offsets for the verify that follows.
 #include "smcsd_launch.cuh"
 
 namespace smcsd {
@@ -61,7 +61,10 @@ __global__ void __launch_bounds__(kPacerThreads) pacer_kernel(const __grid_const
     int i = 0;
     for (; i < p.max_blocks; ++i) {
         for (int j = warp; j < p.b; j += nw) {
-            const uint16_t* h = p.hidden + ((size_t)s * P + (size_t)i * p.b + j) * p.d;
+            const size_t pos = (size_t)i * p.b + j;  // draft position within the sequence
+            const uint16_t* h = p.hidden + ((size_t)s * P + pos) * p.d;
+            // w . (h + e) as w . h + w . e: each bf16 x bf16 product is exact in float
+            const uint16_t* pe = p.pos_emb ? p.pos_emb + pos * p.d : nullptr;
             dd acc{0.0f, 0.0f};
             if (p.vec) {
                 for (int e = lane * 8; e < p.d; e += 256) {
@@ -71,9 +74,17 @@ __global__ void __launch_bounds__(kPacerThreads) pacer_kernel(const __grid_const
                     const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        // bf16 x bf16 products are exact in float
                         acc = dd_add(acc, dd{f_mul(bf16_lo(hw[q]), bf16_lo(ww[q])), 0.0f});
                         acc = dd_add(acc, dd{f_mul(bf16_hi(hw[q]), bf16_hi(ww[q])), 0.0f});
+                    }
+                    if (pe) {
+                        const uint4 ev = __ldg(reinterpret_cast<const uint4*>(pe + e));
+                        const uint32_t ew[4] = {ev.x, ev.y, ev.z, ev.w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            acc = dd_add(acc, dd{f_mul(bf16_lo(ew[q]), bf16_lo(ww[q])), 0.0f});
+                            acc = dd_add(acc, dd{f_mul(bf16_hi(ew[q]), bf16_hi(ww[q])), 0.0f});
+                        }
                     }
                 }
             } else {
@@ -81,6 +92,10 @@ __global__ void __launch_bounds__(kPacerThreads) pacer_kernel(const __grid_const
                     const float hv = __uint_as_float(((uint32_t)__ldg(h + e)) << 16);
                     const float wv = __uint_as_float(((uint32_t)__ldg(p.w + e)) << 16);
                     acc = dd_add(acc, dd{f_mul(hv, wv), 0.0f});
+                    if (pe) {
+                        const float ev = __uint_as_float(((uint32_t)__ldg(pe + e)) << 16);
+                        acc = dd_add(acc, dd{f_mul(ev, wv), 0.0f});
+                    }
                 }
             }
             const dd dot = warp_sum_dd(acc);

@@ -7,7 +7,9 @@
 //         min(1, p/q) in position order, the acceptance length, and the hand-off of the row
 //         (pair) to draw the final token from;
 //   SMC   (same page, sec. 2 steps 3-4 and sec. 3): the log-weight update
-//         sum_k log pi_k(x_k) - log q_k(x_k);
+//         sum_k log pi_k(x_k) - log q_k(x_k), or for the whole-sequence power target
+//         sum_k alpha log p_k(x_k) - log q_k(x_k) + (alpha - 1) log p_K(b), plus an optional
+//         additive log-reward (sec. 3 "flexibility", sec. 5);
 //   step  additionally, per group of N particles: effective sample size, systematic
 //         resampling and the page-table remap with refcounts.
 #pragma once
@@ -44,6 +46,17 @@ __device__ __noinline__ void row_epilogue(const StreamParams& p, const PreciseCt
             if (tok < 0) raise_error(p.ws, kErrNonfinite);
             p.bonus_token[s] = tok < 0 ? 0 : tok;
             if (p.lse_tgt) p.lse_tgt[row] = lse;
+            if (p.target_seq) {
+                // whole-sequence power target: the (K+1)-th token, drawn from p, carries the
+                // weight factor p^(alpha-1), i.e. (alpha - 1) (c z_tok - lse) in log space
+                dd inc{0.0f, 0.0f};
+                if (tok >= 0 && p.alpha != 1.0f) {
+                    const float z = logit_at<DT>(row_ptr<DT>(R.tgt, row, R.V), tok);
+                    const dd lp = dd_sub(dd_mul_f(dd{p.sc_t.c_hi, p.sc_t.c_lo}, z), dd{lse, 0.0f});
+                    inc = dd_mul(lp, two_sum(p.alpha, -1.0f));  // alpha - 1 exactly
+                }
+                sL[slot] = make_float2(inc.hi, inc.lo);
+            }
         }
         return;
     }
@@ -80,22 +93,30 @@ __device__ __forceinline__ void prefetch_token_logit(const StreamParams& p, int 
     sZ[slot] = z;
 }
 
-// log p_k(x_k) - log q_k(x_k) at position k, as a double-float, from the row normalisers sL and
+// log p_k(x_k) and log q_k(x_k) at position k, as double-floats, from the row normalisers sL and
 // the draft token and logits there (sX, sZ) of this sequence's block. False (with an error raised)
 // if the token is out of range.
-__device__ __forceinline__ bool log_ratio(const StreamParams& p, int k, const float2* sL, const int* sX,
-                                          const float* sZ, dd& ell) {
+__device__ __forceinline__ bool log_probs(const StreamParams& p, int k, const float2* sL, const int* sX,
+                                          const float* sZ, dd& lt, dd& ld) {
     const int x = sX[2 * k];
-    ell = dd{0.0f, 0.0f};
+    lt = ld = dd{0.0f, 0.0f};
     if (x < 0 || x >= p.R.V) {
         raise_error(p.ws, kErrRange);
         return false;
     }
     const float2 Lt = sL[2 * k], Ld = sL[2 * k + 1];
-    const dd lt = dd_sub(dd_mul_f(dd{p.sc_t.c_hi, p.sc_t.c_lo}, sZ[2 * k]), dd{Lt.x, Lt.y});
-    const dd ld = dd_sub(dd_mul_f(dd{p.sc_d.c_hi, p.sc_d.c_lo}, sZ[2 * k + 1]), dd{Ld.x, Ld.y});
-    ell = dd_sub(lt, ld);
+    lt = dd_sub(dd_mul_f(dd{p.sc_t.c_hi, p.sc_t.c_lo}, sZ[2 * k]), dd{Lt.x, Lt.y});
+    ld = dd_sub(dd_mul_f(dd{p.sc_d.c_hi, p.sc_d.c_lo}, sZ[2 * k + 1]), dd{Ld.x, Ld.y});
     return true;
+}
+
+// log p_k(x_k) - log q_k(x_k) at position k (0 with an error raised if the token is out of range).
+__device__ __forceinline__ bool log_ratio(const StreamParams& p, int k, const float2* sL, const int* sX,
+                                          const float* sZ, dd& ell) {
+    dd lt, ld;
+    const bool ok = log_probs(p, k, sL, sX, sZ, lt, ld);
+    ell = dd_sub(lt, ld);
+    return ok;
 }
 
 // SD: the ratio tests min(1, p/q) in position order, the acceptance length and the hand-off of
@@ -135,16 +156,28 @@ static __device__ __noinline__ void sd_seq_epilogue(const StreamParams& p, int s
 }
 
 // SMC: log-weight update sum_k log pi_k(x_k) - log q_k(x_k) of particle s (double-float sums),
-// from its old log-weight lw_old.
+// from its old log-weight lw_old. With the whole-sequence power target the terms are
+// alpha log p_k(x_k) - log q_k(x_k), plus the (K+1)-th token's factor that its row epilogue left
+// in sL[2K]; a log-reward adds reward_scale * log_reward[s].
 static __device__ __noinline__ void smc_particle_epilogue(const StreamParams& p, int s, int lane, float lw_old,
                                                           const float2* sL, const int* sX, const float* sZ) {
     dd inc{0.0f, 0.0f};
     for (int k = lane; k < p.R.K; k += kWarp) {
-        dd ell;
-        if (log_ratio(p, k, sL, sX, sZ, ell)) inc = dd_add(inc, ell);
+        dd lt, ld;
+        if (log_probs(p, k, sL, sX, sZ, lt, ld))
+            inc = dd_add(inc, dd_sub(p.target_seq ? dd_mul_f(lt, p.alpha) : lt, ld));
     }
     inc = warp_sum_dd(inc);
     if (lane == 0) {
+        if (p.target_seq) {
+            const float2 b = sL[2 * p.R.K];
+            inc = dd_add(inc, dd{b.x, b.y});
+        }
+        if (p.log_reward) {
+            const float r = __ldg(p.log_reward + s);
+            if (!(fabsf(r) <= 3.402823466e38f)) raise_error(p.ws, kErrNonfinite);  // NaN or inf
+            inc = dd_add(inc, two_prod(p.reward_scale, r));
+        }
         const dd lw = dd_add(dd{lw_old, 0.0f}, inc);
         p.logw[s] = f_add(lw.hi, lw.lo);
     }

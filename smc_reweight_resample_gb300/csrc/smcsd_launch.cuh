@@ -30,6 +30,12 @@ struct StreamParams {
     // SMC outputs
     float* logw;
     int32_t* bonus_token;
+    // SMC tilted targets: whole-sequence power target (sc_t is then 1/T and draft-token log-
+    // probabilities are weighted by alpha, the (K+1)-th token by alpha - 1), additive log-reward
+    bool target_seq;
+    float alpha;
+    const float* log_reward;  // [S] or null
+    float reward_scale;
     // fused SMC step: per-group stage
     int G, N;
     float ess_threshold;
@@ -99,6 +105,7 @@ struct RemapParams {
 struct PacerParams {
     const uint16_t* hidden;
     const uint16_t* w;
+    const uint16_t* pos_emb;  // [max_blocks*b, d] or null
     float c;
     int S, b, max_blocks, d;
     float t0, rho;

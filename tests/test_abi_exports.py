@@ -68,3 +68,26 @@ def test_argument_checks_return_before_any_cuda_call(lib):
     # workspace too small
     assert lib.sd_verify(fake, fake, 1, fake, None, None, 4, 2, 10, 1.0, fake, fake, fake, None,
                          None, fake, 16, None) == -3
+
+
+def test_tilted_and_pos_emb_argument_checks(lib):
+    P, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.smc_reweight_tilted.argtypes = [P, P, i, P, i, i, i, f, f, i, P, f, P, P, P, P, P, P, sz, P]
+    fake = P(256)
+
+    def rw(target, reward, scale, alpha=2.0, ws_bytes=1 << 20):
+        return lib.smc_reweight_tilted(fake, fake, 1, fake, 4, 2, 10, 1.0, alpha, target, reward,
+                                       scale, fake, fake, fake, None, None, fake, ws_bytes, None)
+
+    assert rw(2, None, 0.0) == -1                  # unknown target
+    assert rw(-1, None, 0.0) == -1
+    assert rw(1, fake, float("nan")) == -1         # reward given with a non-finite scale
+    assert rw(1, fake, float("inf")) == -1
+    assert rw(1, None, 0.0, alpha=0.0) == -1       # alpha <= 0
+    assert rw(1, fake, 0.5, ws_bytes=16) == -3     # valid up to the workspace size
+    lib.pacer_block_stop_pos.argtypes = [P, P, P, f, i, i, i, i, f, f, P, P, P, P, P, sz, P]
+    # b above the kernel's limit of 64, and a null head, are refused with or without embeddings
+    assert lib.pacer_block_stop_pos(fake, fake, fake, 0.0, 4, 65, 5, 16, 0.5, 1.1, fake, None,
+                                    None, None, fake, 1 << 20, None) == -1
+    assert lib.pacer_block_stop_pos(fake, None, fake, 0.0, 4, 4, 5, 16, 0.5, 1.1, fake, None,
+                                    None, None, fake, 1 << 20, None) == -1
