@@ -518,6 +518,176 @@ def run_gpu(args):
     return 0
 
 
+# --------------------------------------------------------------------------------------------
+# sweeps (measurement only, not the bench line)
+# --------------------------------------------------------------------------------------------
+
+SWEEP_TEMPERATURES = (0.5, 0.7, 1.0, 1.4, 2.0)
+SWEEP_PARTICLES = (2, 4, 8, 16, 32, 64, 128)
+
+
+def _graph_ms(step, n_steps, stream):
+    """Device ms per call of step(i) replayed from a CUDA graph of NSETS calls."""
+    import torch
+
+    with torch.cuda.stream(stream):
+        for i in range(NSETS):
+            step(i)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(NSETS):
+            step(i)
+    graph.replay()
+    torch.cuda.synchronize()
+    reps = max(1, n_steps // NSETS)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / (reps * NSETS)
+
+
+def sweep_temperature(args):
+    """SD against SMC-SD as the sampling temperature rises ("Faster LLM Inference via Sequential
+    Monte Carlo", sec. 4 "robustness": SD's throughput falls with its acceptance rate while
+    SMC-SD emits K+1 tokens per particle whatever the temperature). On the 8 x 16 particle,
+    K=4, V=128256 bf16 shape: per temperature, SD verify of the 128 sequences (acceptance length,
+    emitted tokens, device time per call) and the fused SMC-SD step (ESS, resampling rate, device
+    time per step), both through the C ABI on the synthetic logits of the workload."""
+    import numpy as np
+    import torch
+
+    from smc_reweight_resample_gb300 import _binding as B
+    from smc_reweight_resample_gb300 import synth
+
+    B.load()
+    cfg = synth.SMC_LLAMA3
+    S, K, V, G, N, P = cfg.S, cfg.K, cfg.V, cfg.G, cfg.N, cfg.pages_per_seq
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(device=dev)
+    rows = []
+    for T in SWEEP_TEMPERATURES:
+        sets = []
+        for i in range(NSETS):
+            tgt, drf = synth.torch_logits_pair(500 + i, S, K, V, cfg.sigma_d, cfg.sigma_t, dev)
+            toks = synth.torch_gumbel_draft_tokens(600 + i, drf, T)
+            sets.append((tgt, drf, toks))
+        usd = [torch.from_numpy(synth.uniforms(7, S * (K + 1), stream=700 + i)).to(dev)
+               for i in range(NSETS)]
+        wsd = B.Workspace(B.OP_SD_VERIFY, S, K, V, dev)
+        acc = [torch.empty(S, dtype=torch.int32, device=dev) for _ in range(NSETS)]
+        tok = torch.empty(S, dtype=torch.int32, device=dev)
+
+        def sd_step(i):
+            t, d, x = sets[i % NSETS]
+            B.sd_verify(t, d, x, S, K, V, T, usd[i % NSETS], ws=wsd, accept_len=acc[i % NSETS],
+                        out_token=tok, stream=stream)
+
+        sd_ms = _graph_ms(sd_step, args.sweep_steps, stream)
+        assert B.check_status(wsd, stream) == 0
+        a = np.concatenate([acc[i].cpu().numpy() for i in range(NSETS)]).astype(np.float64)
+        sd_tokens = float((a + 1).mean())  # accepted drafts + the residual or bonus token
+
+        ws = B.Workspace(B.OP_SMC_STEP, S, K, V, dev)
+        logw = torch.zeros(S, dtype=torch.float32, device=dev)
+        tables = [torch.from_numpy(synth.initial_page_table(S, P)).to(dev),
+                  torch.empty(S * P, dtype=torch.int32, device=dev)]
+        ub = [torch.from_numpy(synth.uniforms(8, S, stream=800 + i)).to(dev) for i in range(NSETS)]
+        ur = [torch.from_numpy(synth.uniforms(8, G, stream=900 + i)).to(dev) for i in range(NSETS)]
+        outs = [dict(bonus_token=torch.empty(S, dtype=torch.int32, device=dev),
+                     ancestors=torch.empty(S, dtype=torch.int32, device=dev),
+                     ess=torch.empty(G, dtype=torch.float32, device=dev),
+                     resampled=torch.empty(G, dtype=torch.int32, device=dev),
+                     refcount=torch.empty(S * P, dtype=torch.int32, device=dev))
+                for _ in range(NSETS)]
+
+        def smc_step(i):
+            t, d, x = sets[i % NSETS]
+            B.smc_step(t, d, x, G, N, K, V, T, cfg.alpha, ub[i % NSETS], logw, cfg.ess_threshold,
+                       ur[i % NSETS], table_in=tables[i % 2], pages_per_seq=P, num_pages=S * P,
+                       ws=ws, table_out=tables[(i + 1) % 2], stream=stream, **outs[i % NSETS])
+
+        smc_ms = _graph_ms(smc_step, args.sweep_steps, stream)
+        assert B.check_status(ws, stream) == 0
+        ess = np.concatenate([o["ess"].cpu().numpy() for o in outs]) / N
+        res = np.concatenate([o["resampled"].cpu().numpy() for o in outs])
+        rows.append({
+            "temperature": T,
+            "sd": {"mean_accept_len": float(a.mean()), "tokens_per_seq_per_call": sd_tokens,
+                   "ms_per_call": sd_ms, "tokens_per_s": S * sd_tokens / (sd_ms / 1e3)},
+            "smc": {"tokens_per_particle_per_step": K + 1, "ms_per_step": smc_ms,
+                    "tokens_per_s": S * (K + 1) / (smc_ms / 1e3),
+                    "mean_ess_over_n": float(ess.mean()), "resample_rate": float(res.mean())},
+        })
+        del sets, wsd, ws
+        torch.cuda.empty_cache()
+    return {"sweep": "temperature", "workload": "8 prompts x 16 particles, K=4, V=128256 bf16",
+            "data": "synthetic: draft ~ N(0,3), target = draft + N(0,1); draft tokens by Gumbel-max "
+                    "at each temperature", "steps_per_point": args.sweep_steps, "rows": rows}
+
+
+def sweep_particles(args):
+    """Error of the importance-weighted estimate against the number of particles ("Faster LLM
+    Inference via Sequential Monte Carlo", sec. 3: L2 bias and MSE fall as O(1/N), L1 bias as
+    O(1/sqrt(N))). A known target on V=8 (context-free rows p_k, q_k, K=2): G groups of N
+    particles each draw their K tokens from q, smc_reweight gives the weights, and each group
+    estimates p_0 by the self-normalised weighted frequencies of its first tokens. Reported per
+    N: the squared bias |E est - p_0|^2 (L2 bias), the mean squared error and the L1 bias."""
+    import numpy as np
+    import torch
+    from scipy.special import softmax
+
+    from smc_reweight_resample_gb300 import _binding as B
+    from smc_reweight_resample_gb300 import synth
+
+    B.load()
+    Vs, Ks = 8, 2
+    rng = np.random.default_rng(11)
+    zd = rng.normal(0, 1.0, (Ks + 1, Vs)).astype(np.float32)
+    zt = (zd + rng.normal(0, 0.8, (Ks + 1, Vs))).astype(np.float32)
+    q = softmax(zd.astype(np.float64), axis=1)
+    p0 = softmax(zt[0].astype(np.float64))
+    rows = []
+    total = 1 << 21  # particles per N
+    for N in SWEEP_PARTICLES:
+        G = total // N
+        S = G * N
+        ux = synth.uniforms(12, S * Ks, stream=N).reshape(S, Ks).astype(np.float64)
+        x = np.stack([np.minimum(np.searchsorted(np.cumsum(q[k]) / q[k].sum(), ux[:, k],
+                                                 side="right"), Vs - 1)
+                      for k in range(Ks)], axis=1).astype(np.int32)
+        tgt = torch.from_numpy(zt).cuda().repeat(S, 1).contiguous()
+        drf = torch.from_numpy(zd[:Ks]).cuda().repeat(S, 1).contiguous()
+        lw = torch.zeros(S, device="cuda")
+        B.smc_reweight(tgt, drf, torch.from_numpy(x.reshape(-1)).cuda(), S, Ks, Vs, 1.0, 1.0,
+                       torch.from_numpy(synth.uniforms(13, S, stream=N)).cuda(), lw)
+        w = np.exp(lw.cpu().numpy().astype(np.float64)).reshape(G, N)
+        onehot = np.eye(Vs)[x[:, 0]].reshape(G, N, Vs)
+        est = (w[:, :, None] * onehot).sum(1) / w.sum(1)[:, None]  # [G, Vs]
+        bias = est.mean(0) - p0
+        rows.append({"N": N, "groups": G, "l2_bias_sq": float((bias ** 2).sum()),
+                     "mse": float(((est - p0) ** 2).sum(1).mean()),
+                     "l1_bias": float(np.abs(bias).sum()),
+                     # what sampling noise alone adds to l2_bias_sq (sum of Var(est) / G)
+                     "l2_bias_sq_noise_floor": float(est.var(0).sum() / G)})
+        del tgt, drf, lw
+        torch.cuda.empty_cache()
+    return {"sweep": "particles", "target": "V=8, K=2, context-free rows; estimate of p_0",
+            "particles_per_point": total, "rows": rows}
+
+
+def run_sweep(args):
+    import torch
+
+    torch.cuda.set_device(0)
+    out = sweep_temperature(args) if args.sweep == "temperature" else sweep_particles(args)
+    print(json.dumps(out), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -532,9 +702,14 @@ def main(argv=None):
                     help="the default is the headline workload; the others are extra measurements")
     ap.add_argument("--ncu-traffic", type=float, default=None,
                     help="dram bytes per launch of the dominant kernel from an ncu capture")
+    ap.add_argument("--sweep", choices=["temperature", "particles"], default=None,
+                    help="print a measurement sweep instead of the bench line")
+    ap.add_argument("--sweep-steps", type=int, default=400)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
+    if args.sweep:
+        return run_sweep(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)
