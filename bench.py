@@ -315,6 +315,23 @@ def run_reference(args):
 # GPU arm
 # --------------------------------------------------------------------------------------------
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest of every rank's x (all ranks get it). One process: x itself."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_rate(world: int, units_per_step: int, steps: int, seconds: float) -> float:
+    """Whole-job rate: the units every rank processed over the slowest rank's time."""
+    return world * units_per_step * steps / seconds
+
+
 def run_gpu(args):
     import numpy as np
     import torch
@@ -437,14 +454,11 @@ def run_gpu(args):
     if ms_flushed is not None:
         ms = ms_flushed
         args.steps = reps * NSETS
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev)
     assert B.check_status(ws, stream) == 0
     ms_per_step = ms / args.steps
     positions = S * (K + 1)
-    value = world * positions * args.steps / (ms / 1000.0)
+    value = aggregate_rate(world, positions, args.steps, ms / 1000.0)
 
     # e2e: inputs from pinned host memory, results back to the host, every step
     e2e = None
@@ -479,12 +493,9 @@ def run_gpu(args):
                     h.copy_(d, non_blocking=True)
         stream.synchronize()
         t1 = time.perf_counter()
-        et = t1 - t0
-        if world > 1:
-            t = torch.tensor([et], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            et = float(t.item())
-        e2e = {"value": world * positions * e_steps / et, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        et = max_over_ranks(t1 - t0, dev)
+        e2e = {"value": aggregate_rate(world, positions, e_steps, et), "unit": UNIT,
+               "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": e_steps,
                "note": "pinned host inputs copied to the device, smc_step through the C ABI, "
                        "results copied back, every step, one stream, no overlap"}
