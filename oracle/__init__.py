@@ -51,13 +51,15 @@ def _load():
             lib.oracle_smc_reweight_tilted.argtypes = [P, P, i, P, i, i, i, f, f, i, P, f, P, P, P,
                                                        P, P, P, P]
             lib.oracle_ess_resample.argtypes = [P, i, i, f, P, P, P, P, P, P]
+            lib.oracle_draft_sample.argtypes = [P, i, i, i, f, P, P, P, P, P]
             lib.oracle_pagetable_remap.argtypes = [P, P, i, i, P, P, i, P, i]
             lib.oracle_pacer_block_stop.argtypes = [P, P, f, i, i, i, i, f, f, P, P, P]
             lib.oracle_pacer_block_stop_pos.argtypes = [P, P, P, f, i, i, i, i, f, f, P, P, P]
             for fn in (lib.oracle_row_lse, lib.oracle_sample_inverse_cdf, lib.oracle_sd_verify,
                        lib.oracle_smc_reweight, lib.oracle_smc_reweight_tilted,
                        lib.oracle_ess_resample, lib.oracle_pagetable_remap,
-                       lib.oracle_pacer_block_stop, lib.oracle_pacer_block_stop_pos):
+                       lib.oracle_pacer_block_stop, lib.oracle_pacer_block_stop_pos,
+                       lib.oracle_draft_sample):
                 fn.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -188,6 +190,22 @@ def smc_reweight_tilted(tgt, drf, draft_tokens, S, K, V, temperature, alpha, uni
     out["status"] = rc
     if raise_on_error:
         _check(rc, "smc_reweight_tilted")
+    return out
+
+
+def draft_sample(logits, R, V, temperature, uniforms, raise_on_error=True):
+    """One token per row from softmax(z/T) by inverse CDF; dict with tokens, logq, lse, margin."""
+    lib = _load()
+    logits = np.ascontiguousarray(logits)
+    uniforms = np.ascontiguousarray(uniforms, dtype=np.float32)
+    out = dict(tokens=np.full(R, -7, np.int32), logq=np.full(R, np.nan), lse=np.full(R, np.nan),
+               margin=np.full(R, np.nan))
+    rc = lib.oracle_draft_sample(_p(logits), _dtype_code(logits), R, V, float(temperature),
+                                 _p(uniforms), _p(out["tokens"]), _p(out["logq"]), _p(out["lse"]),
+                                 _p(out["margin"]))
+    out["status"] = rc
+    if raise_on_error:
+        _check(rc, "draft_sample")
     return out
 
 

@@ -386,6 +386,50 @@ int oracle_smc_reweight(const void* tgt, const void* drf, int dtype, const int32
 }
 
 /* ------------------------------------------------------------------------------------ */
+/* draft-token sampling                                                                  */
+/* ------------------------------------------------------------------------------------ */
+
+/*
+ * [SMC] sec. 2 step 1: the draft model proposes K tokens per particle; each is drawn from
+ * the draft's tempered distribution q = softmax(z_d / T) at its position.  For R draft
+ * rows (row r of a [R, V] buffer) with one uniform each:
+ *     L_r = log sum_i exp(z_{r,i} / T),   q_r(i) = exp(z_{r,i} / T - L_r),
+ *     token[r] = min{ i : sum_{j<=i} q_r(j) > u_r }      (the inverse-CDF draw above),
+ *     logq[r]  = z_{r,token} / T - L_r   (what the verify needs from the draft side).
+ * Optional outputs: logq[R], lse[R], margin[R] (as oracle_sample_inverse_cdf).
+ */
+int oracle_draft_sample(const void* logits, int dtype, int R, int V, float temperature,
+                        const float* uniforms, int32_t* tokens, double* logq, double* lse,
+                        double* margin) {
+    if (!logits || !uniforms || !tokens || R <= 0 || V <= 0) return OR_EINVAL;
+    if (!(temperature > 0.0f) || isinf(temperature)) return OR_EINVAL;
+    if (dtype != 0 && dtype != 1) return OR_EDTYPE;
+    const double scale = 1.0 / (double)temperature;
+    double* r = (double*)malloc(sizeof(double) * (size_t)V);
+    if (!r) return OR_EINVAL;
+    int rc = OR_OK;
+    for (int row = 0; row < R && rc == OR_OK; ++row) {
+        double L;
+        rc = oracle_row_lse(logits, dtype, row, V, scale, &L);
+        if (rc != OR_OK) break;
+        for (int i = 0; i < V; ++i)
+            r[i] = exp(scale * logit_at(logits, dtype, (long long)row * V + i) - L);
+        int tok;
+        double marg;
+        if (oracle_sample_inverse_cdf(r, V, (double)uniforms[row], &tok, &marg) != OR_OK) {
+            rc = OR_ENONFINITE;
+            break;
+        }
+        tokens[row] = tok;
+        if (logq) logq[row] = row_logprob(logits, dtype, row, V, scale, L, tok);
+        if (lse) lse[row] = L;
+        if (margin) margin[row] = marg;
+    }
+    free(r);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------------------ */
 /* effective sample size and systematic resampling                                       */
 /* ------------------------------------------------------------------------------------ */
 
