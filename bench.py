@@ -35,12 +35,14 @@ NSETS = 4
 
 
 DEFAULT_WORKLOAD = "smc_sd_step_8x16_k4_v128256_bf16"
-# name -> (kind, config); "smc": one smc_step per step, "sd": one sd_verify per step
+# name -> (kind, config); "smc": one smc_step per step, "sd": one sd_verify per step, "draft": one
+# draft_sample over the S*K draft rows per step
 WORKLOADS = {
     DEFAULT_WORKLOAD: ("smc", "SMC_LLAMA3"),
     "smc_sd_step_4x64_k8_v151936_bf16_power": ("smc", "SMC_QWEN_POWER"),
     "sd_verify_128_k4_v128256_bf16": ("sd", "SMC_LLAMA3"),
     "sd_verify_16_k4_v32000_bf16": ("sd", None),
+    "draft_sample_512_v128256_bf16": ("draft", "SMC_LLAMA3"),
 }
 
 
@@ -52,31 +54,43 @@ def workload_config(name: str = DEFAULT_WORKLOAD):
         cfg = synth.SMCConfig("sd_mistral_16_k4_v32000", 1, 16, 4, 32000, 3.0, 1.0, 1.0, 1.0, 256)
     else:
         cfg = getattr(synth, cname)
-    big = NSETS * logit_bytes(cfg) > 129e6
+    lb = logit_bytes(cfg, kind)
+    big = NSETS * lb > 129e6
     config = {
         "workload": name, "K": cfg.K, "V": cfg.V, "temperature": cfg.temperature,
-        "positions_per_step": cfg.S * (cfg.K + 1),
-        "l2": (f"inputs larger than L2: {NSETS} rotating logit sets of {logit_bytes(cfg) / 1e6:.1f} MB"
+        "positions_per_step": positions_per_step(cfg, kind),
+        "l2": (f"inputs larger than L2: {NSETS} rotating logit sets of {lb / 1e6:.1f} MB"
                if big else
-               f"{NSETS} rotating logit sets of {logit_bytes(cfg) / 1e6:.1f} MB; L2 flushed (256 MB "
+               f"{NSETS} rotating logit sets of {lb / 1e6:.1f} MB; L2 flushed (256 MB "
                f"write) before every timed graph replay of {NSETS} calls"),
     }
     if kind == "smc":
         config.update({"G": cfg.G, "N": cfg.N, "alpha": cfg.alpha,
                        "ess_threshold": cfg.ess_threshold, "ctx": cfg.ctx, "page": cfg.page})
+    elif kind == "draft":
+        config.update({"rows": cfg.S * cfg.K, "positions": "drafted tokens (one per draft row)"})
     else:
         config.update({"S": cfg.S})
     return cfg, config, kind
 
 
-def logit_bytes(cfg) -> int:
+def logit_bytes(cfg, kind: str = "smc") -> int:
+    if kind == "draft":  # the draft rows only
+        return cfg.S * cfg.K * cfg.V * 2
     return cfg.S * (2 * cfg.K + 1) * cfg.V * 2
+
+
+def positions_per_step(cfg, kind: str = "smc") -> int:
+    """Verified positions (target rows) per step; for the draft sampler, drafted tokens."""
+    return cfg.S * cfg.K if kind == "draft" else cfg.S * (cfg.K + 1)
 
 
 def algorithmic_bytes(cfg, kind: str = "smc") -> int:
     """Bytes one step must move: every logit once, plus tokens, uniforms, weights and tables."""
     if kind == "sd":  # draft tokens, uniforms, accept lengths and tokens out
         return logit_bytes(cfg) + cfg.S * cfg.K * 4 + cfg.S * (cfg.K + 1) * 4 + cfg.S * 8
+    if kind == "draft":  # uniforms in, tokens and log q out
+        return logit_bytes(cfg, kind) + cfg.S * cfg.K * 12
     small = (cfg.S * cfg.K * 4 + cfg.S * 4 + cfg.G * 4 + cfg.S * 4 * 2 + cfg.S * 4 + cfg.G * 8
              + 2 * cfg.S * cfg.pages_per_seq * 4 + cfg.S * cfg.pages_per_seq * 4)
     return logit_bytes(cfg) + small
@@ -92,6 +106,9 @@ KERNEL_NOTE = {
     "sd": "one sd_verify call: the stream over every row, the SD epilogue, the final-token rows "
           "and residual passes with their epilogues; achieved = algorithmic bytes per call / "
           "device time per call",
+    "draft": "one draft_sample call: stream_tma_kernel (precise partials of every row) and "
+             "finish_kernel (one inverse-CDF draw per row); achieved = algorithmic bytes per call "
+             "/ device time per call",
 }
 
 
@@ -341,7 +358,7 @@ def run_gpu(args):
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     cfg, config, kind = workload_config(args.workload)
-    unit_name = "prompt groups" if kind == "smc" else "sequences"
+    unit_name = {"smc": "prompt groups", "sd": "sequences", "draft": "draft rows"}[kind]
     config["parallelism"] = f"replicas x{world} (independent {unit_name} per GPU, no collective)"
 
     base = None
@@ -368,11 +385,14 @@ def run_gpu(args):
         ur = torch.from_numpy(synth.uniforms(rank, G, stream=101 + 2 * i)).to(dev)
         sets.append((tgt, drf, toks, ub, ur))
     torch.cuda.synchronize()
-    ws = B.Workspace(B.OP_SMC_STEP if kind == "smc" else B.OP_SD_VERIFY, S, K, V, dev)
+    ws = (B.Workspace(B.OP_DRAFT_SAMPLE, S * K, 0, V, dev) if kind == "draft" else
+          B.Workspace(B.OP_SMC_STEP if kind == "smc" else B.OP_SD_VERIFY, S, K, V, dev))
+    draft_out = (torch.empty(S * K, dtype=torch.int32, device=dev),
+                 torch.empty(S * K, dtype=torch.float32, device=dev))
     usd = [torch.from_numpy(synth.uniforms(rank, S * (K + 1), stream=300 + i)).to(dev)
            for i in range(NSETS)]
     sd_out = (torch.empty(S, dtype=torch.int32, device=dev), torch.empty(S, dtype=torch.int32, device=dev))
-    small_set = NSETS * logit_bytes(cfg) <= 129e6
+    small_set = NSETS * logit_bytes(cfg, kind) <= 129e6
     flush = torch.empty((256 << 20) if small_set else 0, dtype=torch.uint8, device=dev)
     logw = torch.zeros(S, dtype=torch.float32, device=dev)
     tables = [torch.from_numpy(synth.initial_page_table(S, P)).to(dev),
@@ -388,6 +408,10 @@ def run_gpu(args):
         if kind == "sd":
             B.sd_verify(tgt, drf, toks, S, K, V, cfg.temperature, usd[i % NSETS], ws=ws,
                         accept_len=sd_out[0], out_token=sd_out[1], stream=stream)
+            return
+        if kind == "draft":
+            B.draft_sample(drf, S * K, V, cfg.temperature, usd[i % NSETS][:S * K], ws=ws,
+                           tokens=draft_out[0], logq=draft_out[1], stream=stream)
             return
         B.smc_step(tgt, drf, toks, G, N, K, V, cfg.temperature, cfg.alpha, ub, logw,
                    cfg.ess_threshold, ur, table_in=tables[i % 2], pages_per_seq=P,
@@ -457,7 +481,7 @@ def run_gpu(args):
     ms = max_over_ranks(ms, dev)
     assert B.check_status(ws, stream) == 0
     ms_per_step = ms / args.steps
-    positions = S * (K + 1)
+    positions = positions_per_step(cfg, kind)
     value = aggregate_rate(world, positions, args.steps, ms / 1000.0)
 
     # e2e: inputs from pinned host memory, results back to the host, every step
@@ -522,6 +546,7 @@ def run_gpu(args):
                      "frac_of_8TBps_spec": achieved / 8000.0},
         "cpu_baseline": base, "e2e": e2e,
         "gpu_launches": args.steps * (SD_KERNELS_PER_CALL if kind == "sd" else
+                                      KERNELS_PER_STEP if kind == "draft" else
                                       KERNELS_PER_STEP + (2 if cfg.N > 32 else 0)),
         "clocks": clocks.summary(t_wall0, t_wall1),
     }

@@ -76,6 +76,7 @@ extern "C" {
 #define SMCSD_OP_ESS_RESAMPLE 3
 #define SMCSD_OP_PAGETABLE_REMAP 4
 #define SMCSD_OP_PACER_BLOCK_STOP 5
+#define SMCSD_OP_DRAFT_SAMPLE 6 /* S = number of rows R; K is ignored */
 
 /*
  * Scratch bytes that `op` needs for S sequences (or particles; for the resampling ops S is the
@@ -155,6 +156,22 @@ int smc_reweight_tilted(const void* tgt_logits, const void* drf_logits, int dtyp
                         float alpha, int target, const float* log_reward, float reward_scale,
                         const float* uniforms, float* logw, int32_t* bonus_token,
                         float* lse_tgt, float* lse_drf, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Draft-token sampling ([SMC] sec. 2 step 1: the draft model proposes K tokens per particle,
+ * each drawn from its tempered distribution). For each of R rows of `logits` ([R, V], dtype as
+ * above), with q_r = softmax(z_r / T):
+ *   tokens[r] = the first token whose cumulative q_r exceeds uniforms[r] (inverse CDF, the same
+ *               draw as the verify's final token);
+ *   logq[r]   = log q_r(tokens[r]) (optional, NULL to skip), what a verify needs from the draft;
+ *   lse[r]    = log sum_i exp(z_{r,i} / T) (optional).
+ * uniforms: float [R]; tokens: int32 [R]; logq, lse: float [R]. ws: see
+ * smcsd_workspace_size(SMCSD_OP_DRAFT_SAMPLE, R, 0, V). An all-masked or non-finite row is
+ * SMCSD_ERR_NONFINITE (device side) and its token is reported as 0.
+ */
+int draft_sample(const void* logits, int dtype, int R, int V, float temperature,
+                 const float* uniforms, int32_t* tokens, float* logq, float* lse,
+                 void* ws, size_t ws_bytes, void* stream);
 
 /*
  * Effective sample size and systematic resampling per group of N particles ([SMC] sec. 2

@@ -18,7 +18,8 @@ LIB_PATH = os.path.join(_HERE, "libsmcsd.so")
 OK, ERR_INVALID_ARG, ERR_DTYPE, ERR_WORKSPACE, ERR_CUDA, ERR_NONFINITE, ERR_RANGE, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5, -6, -7
 F32, BF16 = 0, 1
 TARGET_TOKEN, TARGET_SEQUENCE = 0, 1
-OP_SD_VERIFY, OP_SMC_REWEIGHT, OP_SMC_STEP, OP_ESS_RESAMPLE, OP_PAGETABLE_REMAP, OP_PACER_BLOCK_STOP = range(6)
+(OP_SD_VERIFY, OP_SMC_REWEIGHT, OP_SMC_STEP, OP_ESS_RESAMPLE, OP_PAGETABLE_REMAP, OP_PACER_BLOCK_STOP,
+ OP_DRAFT_SAMPLE) = range(7)
 
 _lib = None
 
@@ -58,10 +59,11 @@ def load(path: str = LIB_PATH):
     lib.smc_step_tilted.argtypes = [P, P, i, P, i, i, i, i, f, f, i, P, f, P, P, P, f, P, P, P, P,
                                     P, P, i, P, i, P, sz, P]
     lib.pacer_block_stop_pos.argtypes = [P, P, P, f, i, i, i, i, f, f, P, P, P, P, P, sz, P]
+    lib.draft_sample.argtypes = [P, i, i, i, f, P, P, P, P, P, sz, P]
     for fn in ("smcsd_workspace_init", "smcsd_check_status", "sd_verify", "smc_reweight",
                "smc_ess_resample", "kv_pagetable_remap", "pacer_block_stop", "smc_step",
                "smc_step_static", "smc_reweight_tilted", "smc_step_tilted",
-               "pacer_block_stop_pos"):
+               "pacer_block_stop_pos", "draft_sample"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -179,6 +181,25 @@ def smc_reweight_tilted(tgt_logits, drf_logits, draft_tokens, S, K, V, temperatu
                                     _ptr(lse_drf), w, n, _stream(stream))
     _check(rc, "smc_reweight_tilted")
     return bonus_token
+
+
+def draft_sample(logits, R, V, temperature, uniforms, ws=None, tokens=None, logq=None, lse=None,
+                 stream=None):
+    """One token per row of logits [R, V] from softmax(z/T). Returns (tokens int32 [R], logq
+    float [R] or None); pass logq=False to skip it, lse (float [R]) to get the normalisers."""
+    dev = logits.device
+    ws = ws or Workspace(OP_DRAFT_SAMPLE, R, 0, V, dev)
+    tokens = _out(tokens, (R,), torch.int32, dev)
+    if logq is None:
+        logq = torch.empty(R, dtype=torch.float32, device=dev)
+    elif logq is False:
+        logq = None
+    w, n = ws.args
+    rc = load().draft_sample(_ptr(logits), _dtype_code(logits), R, V, float(temperature),
+                             _ptr(uniforms), _ptr(tokens), _ptr(logq), _ptr(lse), w, n,
+                             _stream(stream))
+    _check(rc, "draft_sample")
+    return tokens, logq
 
 
 def smc_ess_resample(logw, G, N, ess_threshold, uniforms, ws=None, ancestors=None, ess=None,

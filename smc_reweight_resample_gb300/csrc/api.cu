@@ -46,6 +46,9 @@ extern "C" size_t smcsd_workspace_size(int op, int S, int K, int V) {
         case SMCSD_OP_SMC_STEP:
             if (K < 0 || V <= 0) return 0;
             return ws_layout(S, K, V).total;
+        case SMCSD_OP_DRAFT_SAMPLE:
+            if (V <= 0) return 0;
+            return ws_layout(S, 0, V).total;
         case SMCSD_OP_ESS_RESAMPLE:
         case SMCSD_OP_PAGETABLE_REMAP:
         case SMCSD_OP_PACER_BLOCK_STOP:
@@ -147,7 +150,7 @@ static int smc_common(const void* tgt_logits, const void* drf_logits, int dtype,
                       const float* uniforms, float* logw, int32_t* bonus_token,
                       void* ws, size_t ws_bytes, StreamParams& p) {
     if (dtype != SMCSD_F32 && dtype != SMCSD_BF16) return SMCSD_ERR_DTYPE;
-    if (!tgt_logits || !uniforms || !logw || !bonus_token) return SMCSD_ERR_INVALID_ARG;
+    if (!tgt_logits || !uniforms || !bonus_token) return SMCSD_ERR_INVALID_ARG;
     if (S <= 0 || K < 0 || V <= 0) return SMCSD_ERR_INVALID_ARG;
     if (!finite_pos(temperature) || !finite_pos(alpha)) return SMCSD_ERR_INVALID_ARG;
     if (target != SMCSD_TARGET_TOKEN && target != SMCSD_TARGET_SEQUENCE) return SMCSD_ERR_INVALID_ARG;
@@ -193,6 +196,7 @@ extern "C" int smc_reweight_tilted(const void* tgt_logits, const void* drf_logit
                                    const float* uniforms, float* logw, int32_t* bonus_token,
                                    float* lse_tgt, float* lse_drf, void* ws, size_t ws_bytes,
                                    void* stream) {
+    if (!logw) return SMCSD_ERR_INVALID_ARG;
     StreamParams p{};
     int rc = smc_common(tgt_logits, drf_logits, dtype, draft_tokens, S, K, V, temperature, alpha,
                         target, log_reward, reward_scale, uniforms, logw, bonus_token, ws,
@@ -225,7 +229,7 @@ extern "C" int smc_step_tilted(const void* tgt_logits, const void* drf_logits, i
                                int32_t* refcount, int num_pages, void* ws, size_t ws_bytes,
                                void* stream) {
     if (G <= 0 || N <= 0 || (long long)G * N > 0x7fffffffLL) return SMCSD_ERR_INVALID_ARG;
-    if (!resample_uniforms || !ancestors || isnan(ess_threshold)) return SMCSD_ERR_INVALID_ARG;
+    if (!logw || !resample_uniforms || !ancestors || isnan(ess_threshold)) return SMCSD_ERR_INVALID_ARG;
     const bool remap = table_in != nullptr;
     if (remap) {
         if (!table_out || table_out == table_in || pages_per_seq <= 0) return SMCSD_ERR_INVALID_ARG;
@@ -270,6 +274,21 @@ extern "C" int smc_step(const void* tgt_logits, const void* drf_logits, int dtyp
                            bonus_token, ess_threshold, resample_uniforms, ancestors, ess,
                            resampled, table_in, table_out, pages_per_seq, refcount, num_pages,
                            ws, ws_bytes, stream);
+}
+
+extern "C" int draft_sample(const void* logits, int dtype, int R, int V, float temperature,
+                            const float* uniforms, int32_t* tokens, float* logq, float* lse,
+                            void* ws, size_t ws_bytes, void* stream) {
+    // each row is a "particle" with no draft positions: its (K+1)-th token is the draw
+    StreamParams p{};
+    int rc = smc_common(logits, nullptr, dtype, nullptr, R, 0, V, temperature, 1.0f,
+                        SMCSD_TARGET_TOKEN, nullptr, 0.0f, uniforms, nullptr, tokens, ws, ws_bytes,
+                        p);
+    if (rc) return rc;
+    p.mode = kModeSMC;
+    p.lse_tgt = lse;
+    p.bonus_logq = logq;
+    return from_cuda(launch_stream(p, (cudaStream_t)stream));
 }
 
 extern "C" int smc_ess_resample(float* logw, int G, int N, float ess_threshold,

@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(kFinishMaxWarps * kWarp)
     if (ks >= 0) {
         for (int slot = warp; slot < 2 * ks; slot += nw)
             if (lane == 0) prefetch_token_logit<DT>(p, s, slot, sX, sZ);
-        if (MODE != kModeSD && threadIdx.x == 0) lw_old = __ldcg(p.logw + s);
+        if (MODE != kModeSD && threadIdx.x == 0 && p.logw) lw_old = __ldcg(p.logw + s);
         if (MODE == kModeSMCStep && p.table_in && (int)threadIdx.x * 32 < p.pages_per_seq)
             l2_prefetch(p.table_in + (size_t)s * p.pages_per_seq + threadIdx.x * 32);
     }

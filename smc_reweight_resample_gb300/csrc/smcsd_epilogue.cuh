@@ -46,16 +46,21 @@ __device__ __noinline__ void row_epilogue(const StreamParams& p, const PreciseCt
             if (tok < 0) raise_error(p.ws, kErrNonfinite);
             p.bonus_token[s] = tok < 0 ? 0 : tok;
             if (p.lse_tgt) p.lse_tgt[row] = lse;
-            if (p.target_seq) {
-                // whole-sequence power target: the (K+1)-th token, drawn from p, carries the
-                // weight factor p^(alpha-1), i.e. (alpha - 1) (c z_tok - lse) in log space
-                dd inc{0.0f, 0.0f};
-                if (tok >= 0 && p.alpha != 1.0f) {
+            if (p.target_seq || p.bonus_logq) {
+                // log-probability of the drawn token, c z_tok - lse
+                dd lp{0.0f, 0.0f};
+                if (tok >= 0) {
                     const float z = logit_at<DT>(row_ptr<DT>(R.tgt, row, R.V), tok);
-                    const dd lp = dd_sub(dd_mul_f(dd{p.sc_t.c_hi, p.sc_t.c_lo}, z), dd{lse, 0.0f});
-                    inc = dd_mul(lp, two_sum(p.alpha, -1.0f));  // alpha - 1 exactly
+                    lp = dd_sub(dd_mul_f(dd{p.sc_t.c_hi, p.sc_t.c_lo}, z), dd{lse, 0.0f});
                 }
-                sL[slot] = make_float2(inc.hi, inc.lo);
+                if (p.bonus_logq) p.bonus_logq[s] = f_add(lp.hi, lp.lo);
+                if (p.target_seq) {
+                    // whole-sequence power target: the (K+1)-th token, drawn from p, carries
+                    // the weight factor p^(alpha-1), i.e. (alpha - 1) lp in log space
+                    const dd inc = p.alpha != 1.0f ? dd_mul(lp, two_sum(p.alpha, -1.0f))  // exact alpha - 1
+                                                   : dd{0.0f, 0.0f};
+                    sL[slot] = make_float2(inc.hi, inc.lo);
+                }
             }
         }
         return;
@@ -168,7 +173,7 @@ static __device__ __noinline__ void smc_particle_epilogue(const StreamParams& p,
             inc = dd_add(inc, dd_sub(p.target_seq ? dd_mul_f(lt, p.alpha) : lt, ld));
     }
     inc = warp_sum_dd(inc);
-    if (lane == 0) {
+    if (lane == 0 && p.logw) {  // (no log-weights when only the draws are wanted)
         if (p.target_seq) {
             const float2 b = sL[2 * p.R.K];
             inc = dd_add(inc, dd{b.x, b.y});

@@ -36,6 +36,8 @@ struct StreamParams {
     float alpha;
     const float* log_reward;  // [S] or null
     float reward_scale;
+    // log-probability of each particle's drawn (K+1)-th token at the target's scale, or null
+    float* bonus_logq;
     // fused SMC step: per-group stage
     int G, N;
     float ess_threshold;
