@@ -96,13 +96,13 @@ def algorithmic_bytes(cfg, kind: str = "smc") -> int:
     return logit_bytes(cfg) + small
 
 
-KERNELS_PER_STEP = 2  # stream pass and finishing pass (the refcount memset is a copy-engine op);
+KERNELS_PER_STEP = 2  # stream pass (which also zeroes the refcounts) and finishing pass;
 # groups of more than 32 particles add the stand-alone resampling and page-table kernels
 SD_KERNELS_PER_CALL = 6  # stream, epilogue, rows stream and epilogue, residual stream and draw
 KERNEL_NOTE = {
-    "smc": "one smc_step call: stream_tma_kernel, finish_kernel and the 64 KB refcount memset "
-           "(kernel shares in profiles/launches_<workload>.md); achieved = algorithmic bytes per "
-           "step / device time per step",
+    "smc": "one smc_step call: stream_tma_kernel and finish_kernel (kernel shares in "
+           "profiles/launches_<workload>.md); achieved = algorithmic bytes per step / device time "
+           "per step",
     "sd": "one sd_verify call: the stream over every row, the SD epilogue, the final-token rows "
           "and residual passes with their epilogues; achieved = algorithmic bytes per call / "
           "device time per call",

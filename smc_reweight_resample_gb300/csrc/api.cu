@@ -254,10 +254,8 @@ extern "C" int smc_step_tilted(const void* tgt_logits, const void* drf_logits, i
     p.table_in = table_in;
     p.table_out = table_out;
     p.pages_per_seq = pages_per_seq;
-    p.refcount = remap ? refcount : nullptr;
+    p.refcount = remap ? refcount : nullptr;  // zeroed by the streaming pass
     p.num_pages = num_pages;
-    if (p.refcount && cudaMemsetAsync(refcount, 0, (size_t)num_pages * sizeof(int32_t), st) != cudaSuccess)
-        return SMCSD_ERR_CUDA;
     return from_cuda(launch_stream(p, st));
 }
 

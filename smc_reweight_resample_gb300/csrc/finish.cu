@@ -70,6 +70,9 @@ __global__ void __launch_bounds__(kFinishMaxWarps * kWarp)
     }
     const int s = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    // the next kernel on the stream may launch now; a programmatic dependent waits for this
+    // kernel's completion before it touches memory
+    if (threadIdx.x == 0) griddep_launch_dependents();
     const int ks = seq_len(p.R, s, p.ws);
     // what does not depend on the streaming pass is read while it finishes
     float lw_old = 0.0f;

@@ -188,6 +188,15 @@ static __device__ __noinline__ void smc_particle_epilogue(const StreamParams& p,
     }
 }
 
+// The fused step's refcount array set to zero by the streaming pass (grid-stride), so that the
+// finishing pass's remap, which starts only once the stream has completed, counts from zero.
+__device__ __forceinline__ void zero_refcount(const StreamParams& p) {
+    if (!p.refcount) return;
+    const int stride = (int)(gridDim.x * blockDim.x);
+    for (int i = (int)(blockIdx.x * blockDim.x + threadIdx.x); i < p.num_pages; i += stride)
+        p.refcount[i] = 0;
+}
+
 // Page-table rows of one group after resampling, by threads 0..nthr-1 of a block: row j of the output
 // is row anc[j] of the input (row j when the group was not resampled), W ints per access; every
 // non-empty page id is counted in refcount.

@@ -410,6 +410,11 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    // Launched as a programmatic dependent of the kernel before it on the stream (the previous
+    // step's finishing pass, for instance): nothing global is read or written before that kernel
+    // has completed and its writes are visible.
+    griddep_wait();
+    if (MODE == kModeSMCStep) zero_refcount(p);
     if (threadIdx.x == 0) griddep_launch_dependents();
     if (warp < kTmaProducers) {
         constexpr int kPer = kRing / kTmaProducers;
@@ -563,8 +568,20 @@ static cudaError_t launch_tma_t(const StreamParams& p0, cudaStream_t st) {
     const long long want = (units + kTmaConsumers - 1) / kTmaConsumers;
     int grid = (int)(want < cap ? want : cap);
     if (grid < 1) grid = 1;
-    kern<<<grid, kTmaThreads, kSmemBytes, st>>>(p);
-    return cudaGetLastError();
+    // programmatic stream serialisation: the launch and the blocks' set-up overlap the tail of
+    // the kernel before; the kernel's griddepcontrol.wait orders everything else after it
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)kTmaThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void* args[] = {&p};
+    return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(kern), args);
 }
 
 cudaError_t launch_stream_tma(const StreamParams& p, cudaStream_t st) {

@@ -17,6 +17,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     constexpr bool kPrecise = MODE != kModeSD;
     __shared__ Exp2Table sT;
     extern __shared__ __align__(16) float2 sTab[];  // kTabSize entries when the table is used
+    if (MODE == kModeSMCStep) zero_refcount(p);
     load_exp2_table(p.T, sT);
     PreciseCtx P{p.sc_t, &sT, nullptr, p.ws, p.direct};
     if (kPrecise && DT == 1 && p.use_table) {
