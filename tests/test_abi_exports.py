@@ -91,3 +91,18 @@ def test_tilted_and_pos_emb_argument_checks(lib):
                                     None, None, fake, 1 << 20, None) == -1
     assert lib.pacer_block_stop_pos(fake, None, fake, 0.0, 4, 4, 5, 16, 0.5, 1.1, fake, None,
                                     None, None, fake, 1 << 20, None) == -1
+
+
+def test_draft_sample_argument_checks(lib):
+    P, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.draft_sample.argtypes = [P, i, i, i, f, P, P, P, P, P, sz, P]
+    lib.smcsd_workspace_size.restype = ctypes.c_size_t
+    fake = P(256)
+    ok_ws = lib.smcsd_workspace_size(6, 8, 0, 100)
+    assert ok_ws > 0 and ok_ws == lib.smcsd_workspace_size(6, 8, 5, 100)  # K is ignored
+    assert lib.draft_sample(fake, 3, 8, 100, 1.0, fake, fake, None, None, fake, ok_ws, None) == -2
+    assert lib.draft_sample(None, 1, 8, 100, 1.0, fake, fake, None, None, fake, ok_ws, None) == -1
+    assert lib.draft_sample(fake, 1, 8, 100, 1.0, fake, None, None, None, fake, ok_ws, None) == -1
+    assert lib.draft_sample(fake, 1, 0, 100, 1.0, fake, fake, None, None, fake, ok_ws, None) == -1
+    assert lib.draft_sample(fake, 1, 8, 100, 0.0, fake, fake, None, None, fake, ok_ws, None) == -1
+    assert lib.draft_sample(fake, 1, 8, 100, 1.0, fake, fake, None, None, fake, 64, None) == -3
