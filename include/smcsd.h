@@ -97,6 +97,15 @@ int smcsd_check_status(void* ws, void* stream);
 const char* smcsd_status_string(int code);
 
 /*
+ * Diagnostic for the failure path of the bounded waits (no counterpart on the pages): one warp
+ * runs the streaming pass's two pipeline waits against a barrier and a slot tag that nothing
+ * completes, each giving up after limit_us microseconds (1 .. 2000000) and recording
+ * SMCSD_ERR_TIMEOUT in `ws` as a stalled pipeline would. Read it with smcsd_check_status; the
+ * context stays usable. ws: any workspace of at least 4 bytes (zero-filled once, as always).
+ */
+int smcsd_selftest_wait(unsigned int limit_us, void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Speculative-decoding verify ([SMC] sec. 1; [UAG] sec. 1; ragged lengths from [PACER]
  * Methodik 2). For every sequence s, with p = softmax(z_t / T) and q = softmax(z_d / T):
  *   accept draft x_k iff u[s*(K+1)+k] < min(1, p_k(x_k) / q_k(x_k)), k = 0, 1, ... in order;

@@ -60,10 +60,11 @@ def load(path: str = LIB_PATH):
                                     P, P, i, P, i, P, sz, P]
     lib.pacer_block_stop_pos.argtypes = [P, P, P, f, i, i, i, i, f, f, P, P, P, P, P, sz, P]
     lib.draft_sample.argtypes = [P, i, i, i, f, P, P, P, P, P, sz, P]
+    lib.smcsd_selftest_wait.argtypes = [ctypes.c_uint, P, sz, P]
     for fn in ("smcsd_workspace_init", "smcsd_check_status", "sd_verify", "smc_reweight",
                "smc_ess_resample", "kv_pagetable_remap", "pacer_block_stop", "smc_step",
                "smc_step_static", "smc_reweight_tilted", "smc_step_tilted",
-               "pacer_block_stop_pos", "draft_sample"):
+               "pacer_block_stop_pos", "draft_sample", "smcsd_selftest_wait"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -120,6 +121,12 @@ class Workspace:
     @property
     def args(self):
         return ctypes.c_void_p(self.ptr), ctypes.c_size_t(self.nbytes)
+
+
+def selftest_wait(ws: Workspace, limit_us: int, stream=None):
+    """Runs the bounded waits against nothing; check_status(ws) then reports ERR_TIMEOUT."""
+    w, n = ws.args
+    _check(load().smcsd_selftest_wait(int(limit_us), w, n, _stream(stream)), "smcsd_selftest_wait")
 
 
 def check_status(ws: Workspace, stream=None) -> int:

@@ -73,6 +73,13 @@ extern "C" int smcsd_check_status(void* ws, void* stream) {
     return flag;
 }
 
+extern "C" int smcsd_selftest_wait(unsigned int limit_us, void* ws, size_t ws_bytes, void* stream) {
+    if (limit_us == 0 || limit_us > 2000000u) return SMCSD_ERR_INVALID_ARG;
+    int rc = check_ws(ws, ws_bytes, sizeof(int));
+    if (rc) return rc;
+    return from_cuda(launch_wait_selftest(ws, 1000ull * limit_us, (cudaStream_t)stream));
+}
+
 extern "C" const char* smcsd_status_string(int code) {
     switch (code) {
         case SMCSD_OK: return "ok";

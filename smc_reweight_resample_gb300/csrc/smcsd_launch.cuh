@@ -127,6 +127,7 @@ cudaError_t launch_sd_sample(const SampleParams& p, cudaStream_t st);
 cudaError_t launch_resample(const ResampleParams& p, cudaStream_t st);
 cudaError_t launch_remap(const RemapParams& p, cudaStream_t st);
 cudaError_t launch_pacer(const PacerParams& p, cudaStream_t st);
+cudaError_t launch_wait_selftest(void* ws, unsigned long long limit_ns, cudaStream_t st);
 
 int device_sm_count();
 

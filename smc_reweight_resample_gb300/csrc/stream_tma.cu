@@ -90,12 +90,13 @@ __device__ __forceinline__ unsigned long long global_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
-// Wait for the phase of `parity` to complete, for at most kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Wait for the phase of `parity` to complete, for at most `limit_ns`.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (!mbar_try_wait(bar, parity))
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     return true;
 }
 // Slot tags: one 64-bit word per slot, written by the producer once the slot's chunk is on its
@@ -114,9 +115,10 @@ __device__ __forceinline__ unsigned long long tag_load(uint32_t addr) {
     asm volatile("ld.relaxed.cta.shared::cta.b64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
     return v;
 }
-// Wait (at most kWaitLimitNs) until the tag at `addr` reads k or kTagDone; the tag word seen is
+// Wait (at most `limit_ns`) until the tag at `addr` reads k or kTagDone; the tag word seen is
 // left in `seen`.
-__device__ __forceinline__ bool tag_wait(uint32_t addr, uint32_t k, unsigned long long& seen) {
+__device__ __forceinline__ bool tag_wait(uint32_t addr, uint32_t k, unsigned long long& seen,
+                                         unsigned long long limit_ns = kWaitLimitNs) {
     seen = tag_load(addr);
     uint32_t hi = (uint32_t)(seen >> 32);
     if (hi == k || hi == kTagDone) return true;
@@ -126,8 +128,27 @@ __device__ __forceinline__ bool tag_wait(uint32_t addr, uint32_t k, unsigned lon
         seen = tag_load(addr);
         hi = (uint32_t)(seen >> 32);
         if (hi == k || hi == kTagDone) return true;
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     }
+}
+
+// Diagnostic: the pipeline's two waits, run by one warp against a full barrier and a slot tag
+// that nothing completes, each giving up after limit_ns and recording kErrTimeout, as the
+// streaming pass does when its pipeline stalls. No copy is issued, so none is in flight when the
+// kernel returns.
+__global__ void __launch_bounds__(32) wait_selftest_kernel(void* ws, unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ __align__(8) unsigned long long tag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        tag = (unsigned long long)kTagNone << 32;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    const bool got_bar = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar), 0u, limit_ns));
+    unsigned long long seen = 0;
+    const bool got_tag = __all_sync(0xffffffffu, tag_wait(smem_u32(&tag), 0u, seen, limit_ns));
+    if (threadIdx.x == 0 && (!got_bar || !got_tag)) raise_error(ws, kErrTimeout);
 }
 
 // Makes every word of `raw` an input of an (empty) instruction: what follows in program order
@@ -582,6 +603,11 @@ static cudaError_t launch_tma_t(const StreamParams& p0, cudaStream_t st) {
     cfg.numAttrs = 1;
     void* args[] = {&p};
     return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(kern), args);
+}
+
+cudaError_t launch_wait_selftest(void* ws, unsigned long long limit_ns, cudaStream_t st) {
+    wait_selftest_kernel<<<1, 32, 0, st>>>(ws, limit_ns);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_stream_tma(const StreamParams& p, cudaStream_t st) {

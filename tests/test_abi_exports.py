@@ -106,3 +106,14 @@ def test_draft_sample_argument_checks(lib):
     assert lib.draft_sample(fake, 1, 0, 100, 1.0, fake, fake, None, None, fake, ok_ws, None) == -1
     assert lib.draft_sample(fake, 1, 8, 100, 0.0, fake, fake, None, None, fake, ok_ws, None) == -1
     assert lib.draft_sample(fake, 1, 8, 100, 1.0, fake, fake, None, None, fake, 64, None) == -3
+
+
+def test_selftest_wait_argument_checks(lib):
+    P, sz = ctypes.c_void_p, ctypes.c_size_t
+    lib.smcsd_selftest_wait.argtypes = [ctypes.c_uint, P, sz, P]
+    fake = P(256)
+    assert lib.smcsd_selftest_wait(0, fake, 1024, None) == -1          # no limit
+    assert lib.smcsd_selftest_wait(2000001, fake, 1024, None) == -1    # above 2 s
+    assert lib.smcsd_selftest_wait(1000, None, 1024, None) == -1       # no workspace
+    assert lib.smcsd_selftest_wait(1000, fake, 2, None) == -3          # workspace too small
+    assert lib.smcsd_selftest_wait(1000, P(260), 1024, None) == -3     # misaligned

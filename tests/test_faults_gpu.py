@@ -83,3 +83,27 @@ def test_host_argument_errors(smcsd):
     assert e.value.code == smcsd.ERR_WORKSPACE
     with pytest.raises(TypeError):
         smcsd.sd_verify(t.to(torch.float16), d, toks, c.S, c.K, c.V, 1.0, u, ws=ws)
+
+
+def test_bounded_wait_runs_out_and_the_context_survives(smcsd):
+    """The pipeline's waits, run against a barrier and a slot tag that nothing completes, give
+    up after their limit and record ERR_TIMEOUT; the workspace and the context then serve a
+    normal verify, which matches the oracle."""
+    import time
+
+    import oracle
+
+    c, t, d, toks, u = _sd_inputs(3)
+    ws = smcsd.Workspace(smcsd.OP_SD_VERIFY, c.S, c.K, c.V)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    smcsd.selftest_wait(ws, 20000)  # 20 ms per wait
+    assert smcsd.check_status(ws) == smcsd.ERR_TIMEOUT
+    dt = time.perf_counter() - t0
+    assert 0.035 <= dt < 2.0, dt  # both waits ran their 20 ms, and no longer than a bound
+    assert smcsd.check_status(ws) == 0
+    acc, tok = smcsd.sd_verify(t, d, toks, c.S, c.K, c.V, 1.0, u, ws=ws)
+    assert smcsd.check_status(ws) == 0
+    o = oracle.sd_verify(c.tgt, c.drf, c.draft_tokens, c.S, c.K, c.V, 1.0, c.uniforms)
+    np.testing.assert_array_equal(host(acc), o["accept_len"])
+    np.testing.assert_array_equal(host(tok), o["out_token"])
