@@ -43,6 +43,7 @@ WORKLOADS = {
     "sd_verify_128_k4_v128256_bf16": ("sd", "SMC_LLAMA3"),
     "sd_verify_16_k4_v32000_bf16": ("sd", None),
     "draft_sample_512_v128256_bf16": ("draft", "SMC_LLAMA3"),
+    "pacer_ragged_verify_64_v32256_bf16": ("pacer", None),
 }
 
 
@@ -50,6 +51,12 @@ def workload_config(name: str = DEFAULT_WORKLOAD):
     from smc_reweight_resample_gb300 import synth
 
     kind, cname = WORKLOADS[name]
+    if kind == "pacer":  # 64 sequences, blocks of 4 up to 5, d=2048, then the ragged verify
+        cfg = synth.SMCConfig("pacer_ragged_64_v32256", 1, 64, 20, 32256, 3.0, 1.0, 1.0, 1.0, 256)
+        config = {"workload": name, "S": 64, "b": 4, "max_blocks": 5, "d": 2048, "t0": 0.5,
+                  "rho": 1.1, "V": 32256, "temperature": 1.0,
+                  "positions": "verified positions = target rows of the ragged verify, sum(L+1)"}
+        return cfg, config, kind
     if cname is None:  # the Mistral-vocabulary SD verify: 16 sequences, K=4, V=32000
         cfg = synth.SMCConfig("sd_mistral_16_k4_v32000", 1, 16, 4, 32000, 3.0, 1.0, 1.0, 1.0, 256)
     else:
@@ -347,6 +354,144 @@ def max_over_ranks(x: float, device) -> float:
 def aggregate_rate(world: int, units_per_step: int, steps: int, seconds: float) -> float:
     """Whole-job rate: the units every rank processed over the slowest rank's time."""
     return world * units_per_step * steps / seconds
+
+
+def run_pacer(args):
+    """PACER's blockwise stop followed by the ragged verify of the lengths it chose, as one step:
+    pacer_block_stop (which writes the ragged row offsets on the device) then sd_verify over the
+    packed rows. Four input sets (hidden states and the packed logits for the lengths their stop
+    rule yields) rotate through a graph of four steps."""
+    import numpy as np
+    import torch
+
+    from smc_reweight_resample_gb300 import _binding as B
+    from smc_reweight_resample_gb300 import build as _build
+    from smc_reweight_resample_gb300 import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and rank != 0:
+        return 0  # replicas of this extra workload are not timed
+    cfg, config, kind = workload_config(args.workload)
+    torch.cuda.set_device(local)
+    _build.build()
+    B.load()
+    dev = torch.device("cuda", local)
+    S, b, nb, d, V, T = 64, 4, 5, 2048, cfg.V, 1.0
+    Kmax = b * nb
+    sets, pos, alg = [], [], []
+    for i in range(NSETS):
+        cs = synth.pacer_case(200 + i, S=S, b=b, max_blocks=nb, d=d)
+        h = torch.from_numpy(cs.hidden.view(np.int16)).view(torch.bfloat16).to(dev)
+        w = torch.from_numpy(cs.w.view(np.int16)).view(torch.bfloat16).to(dev)
+        L, _, _, _ = B.pacer_block_stop(h, w, cs.c, S, b, nb, d, cs.t0, cs.rho)
+        lengths = L.cpu().numpy().astype(np.int64)
+        tgt_full, drf_full = synth.torch_logits_pair(300 + i, S, Kmax, V, cfg.sigma_d, cfg.sigma_t, dev)
+        it = np.concatenate([s * (Kmax + 1) + np.arange(lengths[s] + 1) for s in range(S)])
+        idr = np.concatenate([s * Kmax + np.arange(lengths[s]) for s in range(S)])
+        tgt = tgt_full[torch.from_numpy(it).to(dev)].contiguous()
+        drf = drf_full[torch.from_numpy(idr).to(dev)].contiguous()
+        del tgt_full, drf_full
+        toks = synth.torch_gumbel_draft_tokens(400 + i, drf, T)
+        u = torch.from_numpy(synth.uniforms(rank, S * (Kmax + 1), stream=500 + i)).to(dev)
+        outs = (torch.empty(S, dtype=torch.int32, device=dev), torch.empty(S * nb, device=dev),
+                torch.empty(S + 1, dtype=torch.int32, device=dev),
+                torch.empty(S + 1, dtype=torch.int32, device=dev))
+        sets.append((h, w, cs, tgt, drf, toks, u, outs))
+        pos.append(int((lengths + 1).sum()))
+        # hidden states up to the stop, the head, every packed logit once, tokens, uniforms, outputs
+        alg.append(int(lengths.sum()) * d * 2 + d * 2 + (tgt.numel() + drf.numel()) * 2
+                   + int(lengths.sum()) * 4 + S * (Kmax + 1) * 4 + S * 4 * 4 + 2 * (S + 1) * 4)
+    torch.cuda.synchronize()
+    ws_p = B.Workspace(B.OP_PACER_BLOCK_STOP, S, 0, 1, dev)
+    ws_v = B.Workspace(B.OP_SD_VERIFY, S, Kmax, V, dev)
+    acc = torch.empty(S, dtype=torch.int32, device=dev)
+    tok = torch.empty(S, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(i):
+        h, w, cs, tgt, drf, toks, u, (L, bs, to, do) = sets[i % NSETS]
+        lib = B.load()
+        wp, n = ws_p.args
+        rc = lib.pacer_block_stop(B._ptr(h), B._ptr(w), float(cs.c), S, b, nb, d, float(cs.t0),
+                                  float(cs.rho), B._ptr(L), B._ptr(bs), B._ptr(to), B._ptr(do),
+                                  wp, n, B._stream(stream))
+        B._check(rc, "pacer_block_stop")
+        B.sd_verify(tgt, drf, toks, S, Kmax, V, T, u, tgt_offsets=to, drf_offsets=do, ws=ws_v,
+                    accept_len=acc, out_token=tok, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, NSETS)):
+            step(i)
+    stream.synchronize()
+    assert B.check_status(ws_p, stream) == 0 and B.check_status(ws_v, stream) == 0
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(NSETS):
+            step(i)
+    graph.replay()
+    torch.cuda.synchronize()
+    total = sum(x[3].numel() * 2 + x[4].numel() * 2 + x[0].numel() * 2 for x in sets)
+    small_set = total <= 129e6
+    flush = torch.empty((256 << 20) if small_set else 0, dtype=torch.uint8, device=dev)
+    reps = max(1, args.steps // NSETS)
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    clocks = ClockSampler(vis.split(",")[local] if vis else local)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    ms = 0.0
+    with torch.cuda.stream(stream):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if small_set:
+            for r in range(reps):
+                flush.fill_(r & 255)
+                e0.record(stream)
+                graph.replay()
+                e1.record(stream)
+                e1.synchronize()
+                ms += e0.elapsed_time(e1)
+        else:
+            e0.record(stream)
+            for _ in range(reps):
+                graph.replay()
+            e1.record(stream)
+            e1.synchronize()
+            ms = e0.elapsed_time(e1)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    time.sleep(0.3)
+    clocks.stop()
+    assert B.check_status(ws_p, stream) == 0 and B.check_status(ws_v, stream) == 0
+    steps = reps * NSETS
+    ms_per_step = ms / steps
+    positions = sum(pos) / NSETS
+    alg_bytes = sum(alg) / NSETS
+    peak, peak_kind = measured_peaks()
+    achieved = alg_bytes / (ms_per_step / 1000.0) / 1e9
+    config.update({"l2": (f"{NSETS} rotating input sets of {total / NSETS / 1e6:.1f} MB on average"
+                          + ("; L2 flushed (256 MB write) before every timed graph replay"
+                             if small_set else ", larger than L2 together")),
+                   "mean_length": positions / S - 1, "positions_per_step": positions})
+    line = {
+        "metric": METRIC, "value": positions / (ms_per_step / 1000.0), "unit": UNIT, "n_gpus": 1,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": config,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "one pacer_block_stop and one ragged sd_verify; achieved = "
+                               "algorithmic bytes per step / device time per step",
+                     "peak_kind": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                     "algorithmic_bytes_per_launch": alg_bytes},
+        "cpu_baseline": None, "e2e": None,
+        "gpu_launches": steps * (1 + SD_KERNELS_PER_CALL),
+        "clocks": clocks.summary(t_wall0, t_wall1),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
 
 
 def run_gpu(args):
@@ -768,6 +913,8 @@ def main(argv=None):
         return run_sweep(args)
     if args.impl == "reference":
         return run_reference(args)
+    if WORKLOADS[args.workload][0] == "pacer":
+        return run_pacer(args)
     return run_gpu(args)
 
 

@@ -43,3 +43,9 @@ def test_recorded_traffic_follows_the_sources():
     assert bench.recorded_traffic(name) == recorded
     # DRAM traffic is the logits read once plus a little: no re-reads
     assert 1.0 <= recorded / bench.algorithmic_bytes(bench.workload_config(name)[0]) < 1.03
+
+
+def test_pacer_workload_config():
+    cfg, config, kind = bench.workload_config("pacer_ragged_verify_64_v32256_bf16")
+    assert kind == "pacer" and config["S"] == 64 and config["V"] == 32256
+    assert config["b"] * config["max_blocks"] == cfg.K == 20
