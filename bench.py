@@ -119,18 +119,28 @@ KERNEL_NOTE = {
 }
 
 
+def _code_only(text: str) -> bytes:
+    """C/C++ source without its comments and with whitespace runs collapsed: what compiles."""
+    import re
+
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split()).encode()
+
+
 def _source_sha256() -> str:
-    """Hash of the CUDA sources and the ABI header, as recorded beside the ncu counters."""
+    """Hash of the code (comments and layout aside) of the CUDA sources and the ABI header, as
+    recorded beside the ncu counters."""
     import hashlib
 
     h = hashlib.sha256()
     d = os.path.join(ROOT, "smc_reweight_resample_gb300", "csrc")
     for f in sorted(os.listdir(d)):
         h.update(f.encode())
-        with open(os.path.join(d, f), "rb") as fh:
-            h.update(fh.read())
-    with open(os.path.join(ROOT, "include", "smcsd.h"), "rb") as fh:
-        h.update(fh.read())
+        with open(os.path.join(d, f), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()))
+    with open(os.path.join(ROOT, "include", "smcsd.h"), encoding="utf-8") as fh:
+        h.update(_code_only(fh.read()))
     return h.hexdigest()
 
 

@@ -11,16 +11,20 @@
  *           (N particles, K drafts each, one target scoring pass, reweighting by the
  *           target/draft probability ratio, resampling when the effective sample size falls
  *           below a threshold, exactly K+1 tokens per particle and step), sec. 3 (page-based
- *           KV: resampling is a metadata update; power sampling as a modified target).
+ *           KV: resampling is a metadata update; power sampling and reward-weighted decoding as
+ *           modified targets; error bounds in N), sec. 5 (reward optimisation and hard
+ *           constraints through the same importance weights).
  *   [PACER] "PACER: Blockwise Pre-verification for Speculative Decoding with Adaptive Length",
- *           Methodik 1-3 (blocks of b drafts, mean estimated acceptance against a threshold t
- *           that is multiplied by rho after each block that passes).
+ *           Methodik 1-3 (blocks of b drafts whose hidden states, with position embeddings, give
+ *           an estimated acceptance; the block mean against a threshold t that is multiplied by
+ *           rho after each block that passes).
  *   [UAG]   "Cross-Family Speculative Decoding for Polish Language Models on Apple Silicon",
  *           sec. 1 (the target verifies k candidates in one pass).
  *
  * Conventions for every entry point
  *   - Every pointer argument is a DEVICE pointer owned by the caller, except where noted. The
- *     library allocates nothing and keeps no state between calls outside the caller's buffers.
+ *     library allocates nothing and keeps no state between calls outside the caller's buffers;
+ *     the one exception is smc_step_static, whose scratch is a device area of the library's own.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream). Every call
  *     only enqueues work on it and returns; results are valid once the stream has reached them.
  *   - Logits are row-major [rows, V] with V contiguous; dtype SMCSD_F32 (float32) or SMCSD_BF16.
