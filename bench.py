@@ -634,6 +634,24 @@ def run_gpu(args):
         ms = ms_flushed
         args.steps = reps * NSETS
     ms = max_over_ranks(ms, dev)
+    # spread of the step time, after the timed region: 200 graph replays, each between its own
+    # events (with the L2 flush before each when the inputs fit in L2)
+    per_step = []
+    with torch.cuda.stream(stream):
+        for r in range(200):
+            if small_set:
+                flush.fill_(r & 255)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+            e1.synchronize()
+            per_step.append(e0.elapsed_time(e1) / NSETS)
+    per_step.sort()
+    spread = {"p10": per_step[20], "median": per_step[100], "p90": per_step[180],
+              "unit": "ms per step", "replays": 200,
+              "note": f"each a graph replay of {NSETS} steps between two events, after the timed region"}
     assert B.check_status(ws, stream) == 0
     ms_per_step = ms / args.steps
     positions = positions_per_step(cfg, kind)
@@ -719,7 +737,7 @@ def run_gpu(args):
                      "peak_kind": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
                      "algorithmic_bytes_per_launch": alg,
                      "frac_of_8TBps_spec": achieved / 8000.0},
-        "cpu_baseline": base, "e2e": e2e,
+        "step_ms_spread": spread, "cpu_baseline": base, "e2e": e2e,
         "gpu_launches": args.steps * (SD_KERNELS_PER_CALL if kind == "sd" else
                                       KERNELS_PER_STEP if kind == "draft" else
                                       KERNELS_PER_STEP + (2 if cfg.N > 32 else 0)),
