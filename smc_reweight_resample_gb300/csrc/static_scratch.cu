@@ -8,18 +8,22 @@
 // file-scope device array of kStaticScratchBytes (32 MiB), set aside when the library's device
 // code is loaded.
 //
-// Per call: the part of the scratch that must start at zero (error flag, completion and claim
-// counters) is cleared on the stream first; when the problem's shape differs from the previous
-// call on this device, the tag of the cached exp table is cleared too, since the table then sits
-// at another offset. The call then runs smc_step on that scratch and, if `status` is given,
-// copies the call's device-side status (0 or a negative SMCSD_* code) there.
+// Placement. The workspace of a call is the last ws_layout(G*N, K, V).total bytes of the area.
+// The cached exp table is the last section of every layout and has the same size for every
+// shape, so it sits at one address for all shapes, and no section of any other shape ever
+// overlaps it: a table published by one call stays intact whatever shapes run in between, and
+// its tag (the scale it was built for) decides alone whether a later call may copy it.
+//
+// Per call: the part of the workspace that must start at zero (error flag, completion and claim
+// counters) is cleared on the stream first. The call then runs smc_step on that workspace and,
+// if `status` is given, copies the call's device-side status (0 or a negative SMCSD_* code)
+// there. No host-side state depends on the shape.
 //
 // Every call on one device uses the same scratch: calls whose device work may overlap (on
 // different streams, or from several host threads without ordering) race on it and give wrong
 // results. The first call on each device looks the scratch's address up (cudaGetSymbolAddress,
 // with that device current); make that first call before any stream capture begins.
 #include <atomic>
-#include <mutex>
 
 #include "smcsd.h"
 #include "smcsd_internal.cuh"
@@ -31,14 +35,7 @@ constexpr int kStaticMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_step_scratch[kStaticScratchBytes];
 
-struct StaticShape {
-    int S, K, V;
-};
-
 static std::atomic<void*> g_scratch_addr[kStaticMaxDevices];
-static std::mutex g_shape_mu;
-static StaticShape g_last_shape[kStaticMaxDevices];
-static bool g_have_shape[kStaticMaxDevices];
 
 // Device address of the scratch on the current device, looked up once per device.
 static int scratch_address(int dev, void** out) {
@@ -49,16 +46,6 @@ static int scratch_address(int dev, void** out) {
     }
     *out = a;
     return SMCSD_OK;
-}
-
-// True if (S, K, V) differs from the previous call's on this device (and records it).
-static bool shape_changed(int dev, int S, int K, int V) {
-    std::lock_guard<std::mutex> lock(g_shape_mu);
-    const StaticShape& last = g_last_shape[dev];
-    const bool changed = !g_have_shape[dev] || last.S != S || last.K != K || last.V != V;
-    g_last_shape[dev] = StaticShape{S, K, V};
-    g_have_shape[dev] = true;
-    return changed;
 }
 
 }  // namespace smcsd
@@ -83,11 +70,10 @@ extern "C" int smc_step_static(const void* tgt_logits, const void* drf_logits, i
     void* ws = nullptr;
     int rc = scratch_address(dev, &ws);
     if (rc) return rc;
+    // the workspace ends where the area ends (L.total is a multiple of 256, so it stays aligned)
+    ws = static_cast<char*>(ws) + (kStaticScratchBytes - L.total);
     cudaStream_t st = (cudaStream_t)stream;
     if (cudaMemsetAsync(ws, 0, L.fast, st) != cudaSuccess) return SMCSD_ERR_CUDA;
-    if (shape_changed(dev, G * N, K, V) &&
-        cudaMemsetAsync(static_cast<char*>(ws) + L.tab, 0, 16, st) != cudaSuccess)
-        return SMCSD_ERR_CUDA;
     rc = smc_step(tgt_logits, drf_logits, dtype, draft_tokens, G, N, K, V, temperature, alpha,
                   bonus_uniforms, logw, bonus_token, ess_threshold, resample_uniforms, ancestors,
                   ess, resampled, table_in, table_out, pages_per_seq, refcount, num_pages, ws,

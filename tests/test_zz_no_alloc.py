@@ -1,9 +1,10 @@
 """smc_step_static (the fused step on the library's own scratch area, no workspace argument)
 against smc_step with a caller workspace, through the C ABI: identical results on consecutive
-calls, including a change of shape between calls, the device-side status of a failing call
-delivered to `status` with the next call clean again, and a shape too large for the area
-rejected before any device work. Kept in the last file collected, so that it also runs after
-every other test in the same process."""
+calls, including a change of shape between calls, a call recorded in a CUDA graph and replayed
+after calls of another shape, the device-side status of a failing call delivered to `status`
+with the next call clean again, and a shape too large for the area rejected before any device
+work. Kept in the last file collected, so that it also runs after every other test in the same
+process."""
 import numpy as np
 import pytest
 import torch
@@ -64,6 +65,67 @@ def test_static_across_a_change_of_shape(smcsd):
         for step in range(2):
             a, b = step_pair(smcsd, cfg, seed, step, lw_ws, lw_st, ws)
             assert_same(a, b, lw_ws, lw_st)
+
+
+def test_static_replayed_after_calls_of_another_shape(smcsd):
+    """A recorded call replayed after calls of a larger shape, whose sections cover where the
+    recorded shape's sections lie, must still match the workspace path: the cached exp table
+    the replay copies may not have been overwritten by the calls in between."""
+    a_cfg, b_cfg = cfg_of(2, 16, 3, 30000, 128), cfg_of(8, 16, 5, 40000, 64)
+    S, K, V, G, N, P = a_cfg.S, a_cfg.K, a_cfg.V, a_cfg.G, a_cfg.N, a_cfg.pages_per_seq
+    x = synth.smc_step_inputs(a_cfg, 41, 0)
+    t, d, toks = dev_logits(x.tgt), dev_logits(x.drf), dev(x.draft_tokens)
+    ub, ur = dev(x.bonus_uniforms), dev(x.resample_uniforms)
+    table = dev(synth.initial_page_table(S, P))
+    lw0 = np.random.default_rng(41).normal(0, 2, S).astype(np.float32)
+    # reference: the workspace path from the same log-weights
+    ws = smcsd.Workspace(smcsd.OP_SMC_STEP, S, K, V)
+    lw_ws = dev(lw0.copy())
+    want = smcsd.smc_step(t, d, toks, G, N, K, V, 1.0, 1.0, ub, lw_ws, N / 2.0, ur, table_in=table,
+                          pages_per_seq=P, num_pages=S * P, ws=ws)
+    assert smcsd.check_status(ws) == 0
+    # eager call of shape A (publishes its table), then the same call recorded in a graph
+    lw_st = dev(lw0.copy())
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    outs = dict(bonus_token=torch.empty(S, dtype=torch.int32, device="cuda"),
+                ancestors=torch.empty(S, dtype=torch.int32, device="cuda"),
+                ess=torch.empty(G, device="cuda"), resampled=torch.empty(G, dtype=torch.int32, device="cuda"),
+                table_out=torch.empty_like(table), refcount=torch.empty(S * P, dtype=torch.int32, device="cuda"))
+
+    def call_a(stream=None):
+        return smcsd.smc_step_static(t, d, toks, G, N, K, V, 1.0, 1.0, ub, lw_st, N / 2.0, ur,
+                                     table_in=table, pages_per_seq=P, num_pages=S * P,
+                                     status=status, stream=stream, **outs)
+
+    call_a()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    stream = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        call_a(stream)
+    torch.cuda.synchronize()
+    # eager calls of shape B in between
+    for step in range(2):
+        y = synth.smc_step_inputs(b_cfg, 42, step)
+        sb = torch.zeros(1, dtype=torch.int32, device="cuda")
+        smcsd.smc_step_static(dev_logits(y.tgt), dev_logits(y.drf), dev(y.draft_tokens), b_cfg.G,
+                              b_cfg.N, b_cfg.K, b_cfg.V, 1.0, 1.0, dev(y.bonus_uniforms),
+                              torch.zeros(b_cfg.S, device="cuda"), b_cfg.N / 2.0,
+                              dev(y.resample_uniforms),
+                              table_in=dev(synth.initial_page_table(b_cfg.S, b_cfg.pages_per_seq)),
+                              pages_per_seq=b_cfg.pages_per_seq,
+                              num_pages=b_cfg.S * b_cfg.pages_per_seq, status=sb)
+        torch.cuda.synchronize()
+        assert int(sb.item()) == 0
+    # replay A from the reference's starting log-weights
+    lw_st.copy_(dev(lw0.copy()))
+    status.fill_(12345)
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert_same(want, outs, lw_ws, lw_st)
 
 
 def test_static_reports_device_status_and_recovers(smcsd):
