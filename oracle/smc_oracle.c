@@ -578,7 +578,9 @@ int oracle_pagetable_remap(const int32_t* ancestors, const int32_t* resampled, i
  * and without one (pos_emb NULL) it is h_j alone.
  * hidden: bf16 [S, max_blocks*b, d]; w: bf16 [d].  block_scores[S*max_blocks] (optional)
  * receives m_i for scored blocks and -1 for blocks after the stop; margin[S] (optional)
- * receives min_i |m_i - t_i| over the comparisons made.
+ * receives min_i |m_i - t_i| over the comparisons made that decide the length: the last
+ * block's comparison is left out, since stopping there and passing there both give
+ * max_blocks*b (INFINITY when no comparison decides it).
  */
 int oracle_pacer_block_stop_pos(const uint16_t* hidden, const uint16_t* w,
                                 const uint16_t* pos_emb, float c, int S, int b, int max_blocks,
@@ -617,7 +619,7 @@ int oracle_pacer_block_stop_pos(const uint16_t* hidden, const uint16_t* w,
             const double mi = msum / (double)b;
             if (block_scores) block_scores[(long long)s * max_blocks + i] = mi;
             double dm = fabs(mi - t);
-            if (dm < mm) mm = dm;
+            if (i < max_blocks - 1 && dm < mm) mm = dm;
             if (mi < t) {
                 len = (i + 1) * b;
                 stopped = 1;

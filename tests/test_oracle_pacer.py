@@ -31,6 +31,7 @@ def test_hand_worked_example(orc):
                                    case["rho"])
         assert out["lengths"][0] == case["length"]
         np.testing.assert_allclose(out["block_scores"], case["block_scores"], atol=1e-12)
+        assert out["margin"][0] == pytest.approx(case["margin"], abs=1e-12)
 
 
 def _zero_head(S, b, nb, d):
