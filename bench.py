@@ -263,10 +263,33 @@ def _group_inputs(cfg, seed: int):
     return _GROUP_CACHE[key]
 
 
-def oracle_positions(cfg, seconds: float, seed: int = 0):
+def cpu_model() -> str:
+    """The host CPU's model name (or the Arm part numbers) from /proc/cpuinfo."""
+    names, parts = [], set()
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                k, v = k.strip(), v.strip()
+                if k in ("model name", "Model Name", "cpu model") and v:
+                    names.append(v)
+                elif k == "CPU part":
+                    parts.add(v)
+    except OSError:
+        return "unknown"
+    if names:
+        return names[0]
+    import platform
+
+    return f"{platform.machine()} (CPU part {', '.join(sorted(parts)) or 'unknown'})"
+
+
+def oracle_positions(cfg, seconds: float, seed: int = 0, threads: int = 1):
     """Runs the float64 oracle on whole particles (and their group's ESS, resampling and
     page-table remap) of the workload for about `seconds` of oracle time, cycling through one
-    pre-generated group of N particles. Returns (positions/s, positions, particles, seconds)."""
+    pre-generated group of N particles. threads == 1: one particle per call; threads > 1: the
+    group's N particles per call, split over `threads` host threads. Returns (positions/s,
+    positions, particles, seconds)."""
     import numpy as np
 
     import oracle
@@ -280,33 +303,50 @@ def oracle_positions(cfg, seconds: float, seed: int = 0):
     positions = 0
     particles = 0
     lw = np.zeros(N, np.float32)
+    per_call = 1 if threads <= 1 else N
     while t_oracle < seconds or particles == 0:
         j = particles % N
-        tgt = x.tgt[j * (K + 1):(j + 1) * (K + 1)]
-        drf = x.drf[j * K:(j + 1) * K]
-        toks = x.draft_tokens[j * K:(j + 1) * K]
+        n = min(per_call, N - j)
+        tgt = x.tgt[j * (K + 1):(j + n) * (K + 1)]
+        drf = x.drf[j * K:(j + n) * K]
+        toks = x.draft_tokens[j * K:(j + n) * K]
         t0 = time.perf_counter()
-        o = oracle.smc_reweight(tgt, drf, toks, 1, K, V, cfg.temperature, cfg.alpha,
-                                x.bonus_uniforms[j:j + 1], lw[j:j + 1])
-        lw[j] = o["logw"][0]
-        if j == N - 1:
+        o = oracle.smc_reweight(tgt, drf, toks, n, K, V, cfg.temperature, cfg.alpha,
+                                x.bonus_uniforms[j:j + n], lw[j:j + n], threads=threads)
+        lw[j:j + n] = o["logw"]
+        if j + n == N:
             r = oracle.ess_resample(lw, 1, N, cfg.ess_threshold, x.resample_uniforms[:1])
             oracle.pagetable_remap(r["ancestors"], r["resampled"], 1, N, table, cfg.pages_per_seq,
                                    num_pages=N * cfg.pages_per_seq)
             lw = r["logw"]
         t_oracle += time.perf_counter() - t0
-        positions += K + 1
-        particles += 1
+        positions += n * (K + 1)
+        particles += n
     return positions / t_oracle, positions, particles, t_oracle
 
 
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
 def cpu_baseline(cfg, seconds=12.0):
-    rate, pos, parts, secs = oracle_positions(cfg, seconds)
-    return {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+    """Two legs of the oracle on the host: every core (the particles of a group split over
+    threads; the line's value) and one thread."""
+    cores = host_cores()
+    model = cpu_model()
+    rate1, pos1, parts1, secs1 = oracle_positions(cfg, seconds / 2)
+    rate, pos, parts, secs = oracle_positions(cfg, seconds / 2, threads=cores)
+    return {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "cpu": model,
             "sample": f"{parts} particles ({pos} positions, {parts * (2 * cfg.K + 1)} rows of "
                       f"{cfg.V} bf16 logits) cycling through one group of {cfg.N} particles of the "
-                      f"same workload, with the group's ESS, resampling and remap; {secs:.1f} s "
-                      f"of single-thread float64 oracle time"}
+                      f"same workload, the group's particles split over {cores} threads, with the "
+                      f"group's ESS, resampling and remap; {secs:.1f} s of float64 oracle time",
+            "single_thread": {"value": rate1, "unit": UNIT, "cores": 1,
+                              "sample": f"{parts1} particles ({pos1} positions) one per call, "
+                                        f"{secs1:.1f} s"}}
 
 
 def run_reference(args):
@@ -318,31 +358,42 @@ def run_reference(args):
         print(json.dumps({"impl": "reference", "unavailable": "the timed oracle leg covers the "
                           "SMC workloads only"}), flush=True)
         return 0
+    config["parallelism"] = parallelism(kind, args.gpus)
+    cores = host_cores()
     budget = 120.0
     per_step = max(0.02, budget / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
-        oracle_positions(cfg, per_step)
-    rates, times, pos_total = [], [], 0
+        oracle_positions(cfg, per_step, threads=cores)
+    pos_total = 0
     t_all = 0.0
     for _ in range(args.steps):
-        rate, pos, parts, secs = oracle_positions(cfg, per_step)
+        rate, pos, parts, secs = oracle_positions(cfg, per_step, threads=cores)
         pos_total += pos
         t_all += secs
     value = pos_total / t_all
+    rate1, pos1, _, secs1 = oracle_positions(cfg, min(10.0, budget / 4))
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * t_all / max(1, args.steps), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config,
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "cpu": cpu_model(),
                          "sample": f"each step: whole particles of the workload for about "
-                                   f"{per_step:.2f} s of single-thread float64 oracle time "
-                                   f"({pos_total} positions in total)"},
+                                   f"{per_step:.2f} s of float64 oracle time, a group's particles "
+                                   f"split over {cores} threads ({pos_total} positions in total)",
+                         "single_thread": {"value": rate1, "unit": UNIT, "cores": 1,
+                                           "sample": f"{pos1} positions, {secs1:.1f} s"}},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def parallelism(kind: str, world: int) -> str:
+    unit_name = {"smc": "prompt groups", "sd": "sequences", "draft": "draft rows"}.get(kind, "units")
+    return f"replicas x{world} (independent {unit_name} per GPU, no collective)"
 
 
 # --------------------------------------------------------------------------------------------
@@ -364,6 +415,67 @@ def max_over_ranks(x: float, device) -> float:
 def aggregate_rate(world: int, units_per_step: int, steps: int, seconds: float) -> float:
     """Whole-job rate: the units every rank processed over the slowest rank's time."""
     return world * units_per_step * steps / seconds
+
+
+def gpu_numa_cpus(gpu_index):
+    """(NUMA node, its CPUs) of the GPU's PCI device, or (None, None) if unknown."""
+    try:
+        bus = subprocess.run(["nvidia-smi", "-i", str(gpu_index), "--query-gpu=pci.bus_id",
+                              "--format=csv,noheader"], capture_output=True, text=True,
+                             timeout=20).stdout.strip()
+        dom, rest = bus.split(":", 1)
+        sysfs = f"/sys/bus/pci/devices/{int(dom, 16):04x}:{rest.lower()}/numa_node"
+        with open(sysfs) as f:
+            node = int(f.read().strip())
+        if node < 0:
+            return None, None
+        with open(f"/sys/devices/system/node/node{node}/cpulist") as f:
+            text = f.read().strip()
+        cpus = set()
+        for part in text.split(","):
+            if not part:
+                continue
+            a, _, b = part.partition("-")
+            cpus.update(range(int(a), int(b or a) + 1))
+        cpus &= os.sched_getaffinity(0)
+        return node, (cpus or None)
+    except Exception:
+        return None, None
+
+
+def h2d_link(dev, nbytes: int, gpu_index) -> dict:
+    """GB/s of a plain host-to-device copy of nbytes from pinned memory (best of 5), with the
+    pinned buffer placed by the default policy, and allocated while the process runs on the
+    CPUs of the GPU's NUMA node (so that its pages land on that node)."""
+    import torch
+
+    def measure():
+        h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+        h.fill_(1)
+        d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        best = float("inf")
+        for _ in range(5):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            d.copy_(h, non_blocking=True)
+            torch.cuda.synchronize()
+            best = min(best, time.perf_counter() - t0)
+        del h, d
+        return nbytes / best / 1e9
+
+    out = {"bytes": nbytes, "default": measure()}
+    node, cpus = gpu_numa_cpus(gpu_index)
+    out["gpu_numa_node"] = node
+    if cpus:
+        all_cpus = os.sched_getaffinity(0)
+        os.sched_setaffinity(0, cpus)
+        try:
+            out["gpu_local_node"] = measure()
+        finally:
+            os.sched_setaffinity(0, all_cpus)
+        out["use_local"] = out["gpu_local_node"] > 1.05 * out["default"]
+        out["local_cpus"], out["all_cpus"] = sorted(cpus), sorted(all_cpus)
+    return out
 
 
 def run_pacer(args):
@@ -513,8 +625,7 @@ def run_gpu(args):
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     cfg, config, kind = workload_config(args.workload)
-    unit_name = {"smc": "prompt groups", "sd": "sequences", "draft": "draft rows"}[kind]
-    config["parallelism"] = f"replicas x{world} (independent {unit_name} per GPU, no collective)"
+    config["parallelism"] = parallelism(kind, world)
 
     base = None
     if rank == 0 and not args.no_cpu_baseline and kind == "smc":
@@ -579,17 +690,30 @@ def run_gpu(args):
             step(i, stream)
     stream.synchronize()
     assert B.check_status(ws, stream) == 0
-    # capture NSETS consecutive steps (an even count keeps the page-table double buffer aligned)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for i in range(NSETS):
-            step(i, stream)
-    torch.cuda.synchronize()
+    # The timed steps are replayed from one CUDA graph of gsteps consecutive steps (a multiple
+    # of NSETS, so that consecutive steps always read different logit sets and the page-table
+    # double buffer stays aligned; up to 256 steps, so that a short run is one replay and not a
+    # string of replays with a launch gap between each); steps beyond a whole number of replays
+    # run eagerly. A second graph of NSETS steps serves the L2-flushed timing of small working
+    # sets and the spread below.
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                step(i, stream)
+        torch.cuda.synchronize()
+        return g
+
+    graph = capture(NSETS)
+    gsteps = NSETS * max(1, min(256, args.steps) // NSETS)
+    big_graph = graph if gsteps == NSETS or small_set else capture(gsteps)
     for _ in range(2):
         graph.replay()
+        if big_graph is not graph:
+            big_graph.replay()
     torch.cuda.synchronize()
 
-    reps, tail = divmod(args.steps, NSETS)
+    reps, tail = divmod(args.steps, gsteps if big_graph is not graph else NSETS)
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
     clocks = ClockSampler(vis.split(",")[local] if vis else local)
     clocks.start()
@@ -618,7 +742,7 @@ def run_gpu(args):
         else:
             ev0.record(stream)
             for _ in range(reps):
-                graph.replay()
+                big_graph.replay()
             for i in range(tail):
                 step(i, stream)
             ev1.record(stream)
@@ -661,6 +785,12 @@ def run_gpu(args):
     e2e = None
     if not args.no_e2e and kind == "smc":
         e_steps = min(args.steps, args.e2e_steps)
+        # the host link: a plain pinned copy of one step's input bytes, with the pinned buffer
+        # placed by the default policy and placed on the GPU's own NUMA node; the faster
+        # placement then holds the e2e host buffers
+        link = h2d_link(dev, logit_bytes(cfg), vis.split(",")[local] if vis else local)
+        if link.get("use_local"):
+            os.sched_setaffinity(0, link["local_cpus"])
         host_sets = []
         for i in range(2):
             tgt, drf, toks, ub, ur = sets[i]
@@ -715,7 +845,10 @@ def run_gpu(args):
                "d2h_bytes_per_step": d2h, "steps": e_steps,
                "note": "pinned host inputs copied to the device, smc_step through the C ABI, "
                        "results copied back, every step; the copies of step i+1 (own stream) "
-                       "overlap the compute of step i"}
+                       "overlap the compute of step i",
+               "h2d_copy_GBps": {k: v for k, v in link.items() if k not in ("local_cpus", "all_cpus")}}
+        if link.get("use_local"):
+            os.sched_setaffinity(0, link["all_cpus"])
 
     if world > 1:
         dist.destroy_process_group()

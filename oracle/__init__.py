@@ -13,6 +13,7 @@ import ctypes
 import os
 import subprocess
 import threading
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
@@ -69,6 +70,39 @@ def _p(a):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
 
+def _q(a, offset):
+    """Pointer to element `offset` of a contiguous array (None stays None)."""
+    return None if a is None else ctypes.c_void_p(a.ctypes.data + int(offset) * a.itemsize)
+
+
+def _blocks(n, threads):
+    """Contiguous blocks [s0, s1) covering range(n), one per thread."""
+    t = max(1, min(int(threads), n))
+    edges = [n * i // t for i in range(t + 1)]
+    return [(edges[i], edges[i + 1]) for i in range(t) if edges[i + 1] > edges[i]]
+
+
+def _run_blocks(n, threads, fn):
+    """Runs fn(s0, s1) over the blocks, in threads when threads > 1 (ctypes releases the GIL
+    for the C call, so the blocks run in parallel), and returns the first nonzero status in
+    block order, which is the status a single call over all of range(n) returns: every
+    sequence or particle is computed on its own, so the split changes no result."""
+    blocks = _blocks(n, threads)
+    if len(blocks) == 1:
+        return fn(*blocks[0])
+    with ThreadPoolExecutor(max_workers=len(blocks)) as ex:
+        rcs = list(ex.map(lambda b: fn(*b), blocks))
+    for rc in rcs:
+        if rc != OK:
+            return rc
+    return OK
+
+
+def default_threads() -> int:
+    """Threads for the heavy oracle calls of the tests: every host core."""
+    return os.cpu_count() or 1
+
+
 def _dtype_code(logits: np.ndarray) -> int:
     if logits.dtype == np.float32:
         return 0
@@ -106,9 +140,10 @@ def sample_inverse_cdf(r: np.ndarray, u: float):
 
 
 def sd_verify(tgt, drf, draft_tokens, S, K, V, temperature, uniforms, tgt_offsets=None,
-              drf_offsets=None, raise_on_error=True):
+              drf_offsets=None, raise_on_error=True, threads=1):
     """Returns a dict with accept_len, out_token, lse_tgt, lse_drf, accept_margin,
-    token_margin and status."""
+    token_margin and status. ``threads`` > 1 splits the sequences into contiguous blocks run
+    in parallel; the results are the same bits."""
     lib = _load()
     tgt = np.ascontiguousarray(tgt)
     drf = np.ascontiguousarray(drf)
@@ -125,10 +160,20 @@ def sd_verify(tgt, drf, draft_tokens, S, K, V, temperature, uniforms, tgt_offset
         lse_tgt=np.full(rows_t, np.nan), lse_drf=np.full(rows_d, np.nan),
         accept_margin=np.full(max(S * K, 1), -1.0), token_margin=np.full(S, np.nan),
     )
-    rc = lib.oracle_sd_verify(_p(tgt), _p(drf), dt, _p(draft_tokens), _p(to), _p(do), S, K, V,
-                              float(temperature), _p(uniforms), _p(out["accept_len"]),
-                              _p(out["out_token"]), _p(out["lse_tgt"]), _p(out["lse_drf"]),
-                              _p(out["accept_margin"]), _p(out["token_margin"]))
+    ragged = to is not None
+
+    def block(s0, s1):
+        # fixed layout: row and token offsets follow s; ragged: the offsets stay absolute
+        tr, dr = (0, 0) if ragged else (s0 * (K + 1) * V, s0 * K * V)
+        tk = 0 if ragged else s0 * K
+        lt, ld = (0, 0) if ragged else (s0 * (K + 1), s0 * K)
+        return lib.oracle_sd_verify(
+            _q(tgt, tr), _q(drf, dr), dt, _q(draft_tokens, tk), _q(to, s0), _q(do, s0), s1 - s0,
+            K, V, float(temperature), _q(uniforms, s0 * (K + 1)), _q(out["accept_len"], s0),
+            _q(out["out_token"], s0), _q(out["lse_tgt"], lt), _q(out["lse_drf"], ld),
+            _q(out["accept_margin"], s0 * K), _q(out["token_margin"], s0))
+
+    rc = _run_blocks(S, threads, block)
     out["status"] = rc
     if raise_on_error:
         _check(rc, "sd_verify")
@@ -136,8 +181,10 @@ def sd_verify(tgt, drf, draft_tokens, S, K, V, temperature, uniforms, tgt_offset
 
 
 def smc_reweight(tgt, drf, draft_tokens, S, K, V, temperature, alpha, uniforms, logw,
-                 raise_on_error=True):
-    """``logw`` (float32 [S]) is copied, updated and returned in the dict."""
+                 raise_on_error=True, threads=1):
+    """``logw`` (float32 [S]) is copied, updated and returned in the dict. ``threads`` > 1
+    splits the particles into contiguous blocks run in parallel; the results are the same
+    bits."""
     lib = _load()
     tgt = np.ascontiguousarray(tgt)
     drf = np.ascontiguousarray(drf)
@@ -150,10 +197,14 @@ def smc_reweight(tgt, drf, draft_tokens, S, K, V, temperature, alpha, uniforms, 
         lse_drf=np.full(max(S * K, 1), np.nan), bonus_margin=np.full(S, np.nan),
         dlogw=np.full(S, np.nan),
     )
-    rc = lib.oracle_smc_reweight(_p(tgt), _p(drf), dt, _p(draft_tokens), S, K, V,
-                                 float(temperature), float(alpha), _p(uniforms), _p(lw),
-                                 _p(out["bonus_token"]), _p(out["lse_tgt"]), _p(out["lse_drf"]),
-                                 _p(out["bonus_margin"]), _p(out["dlogw"]))
+    def block(s0, s1):
+        return lib.oracle_smc_reweight(
+            _q(tgt, s0 * (K + 1) * V), _q(drf, s0 * K * V), dt, _q(draft_tokens, s0 * K), s1 - s0,
+            K, V, float(temperature), float(alpha), _q(uniforms, s0), _q(lw, s0),
+            _q(out["bonus_token"], s0), _q(out["lse_tgt"], s0 * (K + 1)),
+            _q(out["lse_drf"], s0 * K), _q(out["bonus_margin"], s0), _q(out["dlogw"], s0))
+
+    rc = _run_blocks(S, threads, block)
     out["status"] = rc
     if raise_on_error:
         _check(rc, "smc_reweight")
@@ -165,7 +216,7 @@ TARGET_TOKEN, TARGET_SEQUENCE = 0, 1
 
 def smc_reweight_tilted(tgt, drf, draft_tokens, S, K, V, temperature, alpha, uniforms, logw,
                         target_mode=TARGET_TOKEN, log_reward=None, reward_scale=0.0,
-                        raise_on_error=True):
+                        raise_on_error=True, threads=1):
     """Reweight with the per-position (TARGET_TOKEN) or whole-sequence (TARGET_SEQUENCE) power
     target and an optional additive log-reward; same dict as ``smc_reweight``."""
     lib = _load()
@@ -181,28 +232,35 @@ def smc_reweight_tilted(tgt, drf, draft_tokens, S, K, V, temperature, alpha, uni
         lse_drf=np.full(max(S * K, 1), np.nan), bonus_margin=np.full(S, np.nan),
         dlogw=np.full(S, np.nan),
     )
-    rc = lib.oracle_smc_reweight_tilted(_p(tgt), _p(drf), dt, _p(draft_tokens), S, K, V,
-                                        float(temperature), float(alpha), int(target_mode), _p(rw),
-                                        float(reward_scale), _p(uniforms), _p(lw),
-                                        _p(out["bonus_token"]), _p(out["lse_tgt"]),
-                                        _p(out["lse_drf"]), _p(out["bonus_margin"]),
-                                        _p(out["dlogw"]))
+    def block(s0, s1):
+        return lib.oracle_smc_reweight_tilted(
+            _q(tgt, s0 * (K + 1) * V), _q(drf, s0 * K * V), dt, _q(draft_tokens, s0 * K), s1 - s0,
+            K, V, float(temperature), float(alpha), int(target_mode), _q(rw, s0),
+            float(reward_scale), _q(uniforms, s0), _q(lw, s0), _q(out["bonus_token"], s0),
+            _q(out["lse_tgt"], s0 * (K + 1)), _q(out["lse_drf"], s0 * K),
+            _q(out["bonus_margin"], s0), _q(out["dlogw"], s0))
+
+    rc = _run_blocks(S, threads, block)
     out["status"] = rc
     if raise_on_error:
         _check(rc, "smc_reweight_tilted")
     return out
 
 
-def draft_sample(logits, R, V, temperature, uniforms, raise_on_error=True):
+def draft_sample(logits, R, V, temperature, uniforms, raise_on_error=True, threads=1):
     """One token per row from softmax(z/T) by inverse CDF; dict with tokens, logq, lse, margin."""
     lib = _load()
     logits = np.ascontiguousarray(logits)
     uniforms = np.ascontiguousarray(uniforms, dtype=np.float32)
     out = dict(tokens=np.full(R, -7, np.int32), logq=np.full(R, np.nan), lse=np.full(R, np.nan),
                margin=np.full(R, np.nan))
-    rc = lib.oracle_draft_sample(_p(logits), _dtype_code(logits), R, V, float(temperature),
-                                 _p(uniforms), _p(out["tokens"]), _p(out["logq"]), _p(out["lse"]),
-                                 _p(out["margin"]))
+    def block(r0, r1):
+        return lib.oracle_draft_sample(
+            _q(logits, r0 * V), _dtype_code(logits), r1 - r0, V, float(temperature),
+            _q(uniforms, r0), _q(out["tokens"], r0), _q(out["logq"], r0), _q(out["lse"], r0),
+            _q(out["margin"], r0))
+
+    rc = _run_blocks(R, threads, block)
     out["status"] = rc
     if raise_on_error:
         _check(rc, "draft_sample")
