@@ -31,7 +31,8 @@ def run_sd(smcsd, c, ledger, unaligned=False):
     assert smcsd.check_status(ws) == 0
     o = oracle.sd_verify(c.tgt, c.drf if c.drf.size else np.zeros((1, V), c.tgt.dtype),
                          c.draft_tokens if c.draft_tokens.size else np.zeros(1, np.int32), S, K, V,
-                         c.temperature, c.uniforms, c.tgt_offsets, c.drf_offsets)
+                         c.temperature, c.uniforms, c.tgt_offsets, c.drf_offsets,
+                         threads=oracle.default_threads())
     ga, gt = host(acc), host(tok)
     oa, ot = o["accept_len"], o["out_token"]
     if K > 0:
@@ -108,6 +109,24 @@ def test_sd_identical_models_accept_all(smcsd):
 def test_sd_ragged(smcsd):
     lengths = np.array([4, 8, 12, 16, 20, 4, 0, 7, 1, 20, 5, 9], np.int32)
     c = synth.ragged_sd_case(11, lengths, 32256, K_max=20)
+    L = DecisionLedger()
+    run_sd(smcsd, c, L)
+    L.finish()
+
+
+def test_sd_llama3_vocab_128_sequences(smcsd):
+    """The benchmarked SD shape: 128 sequences, K=4, V=128256 bf16 (63 chunks per row in the
+    final-token passes), two seeds."""
+    L = DecisionLedger()
+    for seed in range(2):
+        run_sd(smcsd, synth.sd_case(40 + seed, 128, 4, 128256, 3.0, 1.0, 1.0, "bf16"), L)
+    L.finish()
+
+
+def test_sd_ragged_llama3_vocab(smcsd):
+    """Ragged lengths 0..20 at V=128256."""
+    lengths = np.array([4, 8, 12, 16, 20, 4, 0, 7, 1, 20, 5, 9, 13, 2, 17, 6], np.int32)
+    c = synth.ragged_sd_case(12, lengths, 128256, K_max=20)
     L = DecisionLedger()
     run_sd(smcsd, c, L)
     L.finish()

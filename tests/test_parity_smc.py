@@ -29,7 +29,8 @@ def check_reweight(smcsd, c, u, lw0, T, alpha, ledger):
     tok = smcsd.smc_reweight(dev_logits(c.tgt), dev_logits(c.drf), dev(c.draft_tokens), S, K, V, T,
                              alpha, dev(u), lw, ws=ws, lse_tgt=lse_t, lse_drf=lse_d)
     assert smcsd.check_status(ws) == 0
-    o = oracle.smc_reweight(c.tgt, c.drf, c.draft_tokens, S, K, V, T, alpha, u, lw0)
+    o = oracle.smc_reweight(c.tgt, c.drf, c.draft_tokens, S, K, V, T, alpha, u, lw0,
+                            threads=oracle.default_threads())
     np.testing.assert_allclose(host(lw), o["logw"], atol=FLOAT_ATOL, rtol=0)
     ledger.compare("bonus_token", host(tok), o["bonus_token"], o["bonus_margin"])
     np.testing.assert_allclose(host(lse_t), o["lse_tgt"], atol=FLOAT_ATOL, rtol=0)
@@ -144,6 +145,7 @@ def run_steps(smcsd, cfg, steps, seed=0, teacher_forced=True):
     lw_free = np.zeros(S, np.float32)
     table_free = synth.initial_page_table(S, P)
     first_div = None
+    nthr = oracle.default_threads()
     L = DecisionLedger()
     for step in range(steps):
         x = synth.smc_step_inputs(cfg, seed, step)
@@ -156,7 +158,7 @@ def run_steps(smcsd, cfg, steps, seed=0, teacher_forced=True):
         assert smcsd.check_status(ws) == 0
         # teacher-forced oracle step from the GPU's state
         o = oracle.smc_reweight(x.tgt, x.drf, x.draft_tokens, S, K, V, cfg.temperature, cfg.alpha,
-                                x.bonus_uniforms, lw_before)
+                                x.bonus_uniforms, lw_before, threads=nthr)
         L.compare("bonus_token", host(out["bonus_token"]), o["bonus_token"], o["bonus_margin"])
         r = oracle.ess_resample(o["logw"], G, N, cfg.ess_threshold, x.resample_uniforms)
         compare_resample(L, host(out["ancestors"]), host(out["ess"]), host(out["resampled"]),
@@ -168,7 +170,7 @@ def run_steps(smcsd, cfg, steps, seed=0, teacher_forced=True):
         assert m["refcount"].sum() == S * P
         # free-running oracle
         of = oracle.smc_reweight(x.tgt, x.drf, x.draft_tokens, S, K, V, cfg.temperature,
-                                 cfg.alpha, x.bonus_uniforms, lw_free)
+                                 cfg.alpha, x.bonus_uniforms, lw_free, threads=nthr)
         rf = oracle.ess_resample(of["logw"], G, N, cfg.ess_threshold, x.resample_uniforms)
         mf = oracle.pagetable_remap(rf["ancestors"], rf["resampled"], G, N, table_free, P,
                                     num_pages=S * P)
@@ -190,10 +192,16 @@ def test_smc_step_32_steps(smcsd):
     np.testing.assert_allclose(lw_gpu, lw_free, atol=FLOAT_ATOL, rtol=0)
 
 
-@pytest.mark.parametrize("cfg", [synth.SMC_LLAMA3, synth.SMC_QWEN_POWER], ids=lambda c: c.name)
-def test_smc_step_full_size(smcsd, cfg):
-    first_div, _, _ = run_steps(smcsd, cfg, 2)
-    assert first_div is None
+@pytest.mark.parametrize("cfg,steps", [(synth.SMC_LLAMA3, 32), (synth.SMC_QWEN_POWER, 8)],
+                         ids=["smc_llama3_32_steps", "smc_qwen_power_8_steps"])
+def test_smc_step_full_size(smcsd, cfg, steps):
+    """The full-size workloads run free: 32 consecutive fused steps of the 8 x 16 particle,
+    K=4, V=128256 step and 8 of the 4 x 64, K=8, V=151936 power-target step, each compared
+    with the oracle teacher-forced, and a free-running oracle that must take every decision the
+    GPU took (tokens, resampling flags, ancestors) and end on the same log-weights."""
+    first_div, lw_gpu, lw_free = run_steps(smcsd, cfg, steps)
+    assert first_div is None, f"free-running oracle diverged at step {first_div}"
+    np.testing.assert_allclose(lw_gpu, lw_free, atol=FLOAT_ATOL, rtol=0)
 
 
 @pytest.mark.parametrize("GN", [(8, 16), (3, 48)], ids=["groups_of_16", "groups_of_48"])
