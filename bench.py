@@ -281,7 +281,9 @@ def cpu_model() -> str:
         return names[0]
     import platform
 
-    return f"{platform.machine()} (CPU part {', '.join(sorted(parts)) or 'unknown'})"
+    known = {"0xd4f": "Arm Neoverse V2"}  # MIDR part number of the Neoverse V2 core
+    desc = ", ".join(known.get(p.lower(), f"CPU part {p}") for p in sorted(parts)) or "unknown"
+    return f"{platform.machine()} ({desc})"
 
 
 def oracle_positions(cfg, seconds: float, seed: int = 0, threads: int = 1):

@@ -35,23 +35,36 @@ def _flags():
             "-I", INCLUDE, "-I", CSRC, "--expt-relaxed-constexpr"]
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+def _stale(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "smcsd.h")]
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and not _stale():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+# The library with the opt-in device self-checks (-DSMCSD_CHECKS): every check site records its
+# code and the offending value in the workspace instead of making the access. Built on request
+# (build_checks) into its own folder, for the tests that run the parity cases against it.
+CHECKS_BUILD = os.path.join(HERE, "_build_checks")
+CHECKS_LIB = os.path.join(CHECKS_BUILD, "libsmcsd_checks.so")
+
+
+def build_checks(force: bool = False, verbose: bool = False) -> str:
+    return build(force, verbose, extra_flags=("-DSMCSD_CHECKS",), out=CHECKS_LIB,
+                 objdir=CHECKS_BUILD)
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags=(), out: str = LIB,
+          objdir: str = BUILD) -> str:
+    if not force and not _stale(out):
+        return out
+    os.makedirs(objdir, exist_ok=True)
     cc = nvcc()
     procs = []
     objs = []
     for src in SOURCES:
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(objdir, src.replace(".cu", ".o"))
         objs.append(obj)
         cmd = [cc, *_flags(), *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
@@ -59,17 +72,17 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
     failed = []
     for src, pr in procs:
-        out, _ = pr.communicate()
+        log, _ = pr.communicate()
         if verbose or pr.returncode != 0:
-            sys.stdout.write(out.decode(errors="replace"))
+            sys.stdout.write(log.decode(errors="replace"))
         if pr.returncode != 0:
             failed.append(src)
     if failed:
         raise RuntimeError(f"nvcc failed for {failed}")
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = out + f".tmp{os.getpid()}"
     subprocess.check_call([cc, *ARCH, "-shared", "-o", tmp, *objs])
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":

@@ -30,6 +30,10 @@ def smcsd():
         pytest.skip("no CUDA device")
     from smc_reweight_resample_gb300 import _binding, build
 
-    build.build()
-    _binding.load()
+    alt = os.environ.get("SMCSD_TEST_LIB")  # another build of the library (the self-check build)
+    if alt:
+        _binding.load(alt)
+    else:
+        build.build()
+        _binding.load()
     return _binding
