@@ -2,6 +2,7 @@
 // layer (api.cu) calls.
 #pragma once
 
+#include "smcsd_deal.h"
 #include "smcsd_sampling.cuh"
 
 namespace smcsd {
@@ -38,6 +39,10 @@ struct StreamParams {
     float reward_scale;
     // log-probability of each particle's drawn (K+1)-th token at the target's scale, or null
     float* bonus_logq;
+    // draft log-probabilities log q_k(x_k) given by the caller ([S*K], e.g. from the draft
+    // sampler) in place of the draft logits: the draft rows are then neither streamed nor
+    // normalised (SMC modes only)
+    const float* drf_logq;
     // fused SMC step: per-group stage
     int G, N;
     float ess_threshold;
@@ -61,6 +66,7 @@ struct StreamParams {
     // are sampled) and the fast chunks (all other rows, fslots per sequence) as separate lists
     long long n_precise, n_fast;
     int fslots;
+    int fper;              // fast chunks paired with each precise chunk (smcsd_deal.h)
     FastDiv div_fseq;      // by fslots * cpr
 };
 

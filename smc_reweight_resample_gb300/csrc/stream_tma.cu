@@ -11,15 +11,16 @@
 // the whole ring stays in flight; a precise chunk, read from the slot twice, keeps it until done. Every
 // logit crosses HBM exactly once.
 //
-// Chunks are dealt from two lists, each round-robin over the B blocks: the precise chunks (the
-// rows that are sampled, one per particle) and the fast chunks (all other rows). Block b takes
-// chunks b, b+B, b+2B, ... of the precise list and B-1-b, 2B-1-b, ... of the fast list (so the
-// blocks left with one precise chunk more get no extra fast chunk), puts the precise chunks the
-// fast ones cannot pair up first, then interleaves one precise chunk to fslots fast ones, and
-// ends on the fast chunks left over: every block gets the same share of each kind spread evenly
-// over the pass and finishes on cheap chunks, without a shared counter (a claim from one would
-// put an atomic round trip on the producer's path). The producer lane of slot j loads the
-// block's local chunks 32 * round + j.
+// Chunks are dealt from two lists, each round-robin over the B blocks (smcsd_deal.h): the precise
+// chunks (the rows that are sampled, one per particle) and the fast chunks (all other rows). Block
+// b takes chunks b, b+B, b+2B, ... of the precise list and B-1-b, 2B-1-b, ... of the fast list (so
+// the blocks left with one precise chunk more get no extra fast chunk), puts the precise chunks
+// the fast ones cannot pair up first, then interleaves one precise chunk to fper fast ones (three
+// quarters of the fast rows per sampled row), and ends on the fast chunks left over: every block
+// gets the same share of each kind, the precise ones over the first four fifths of the pass, and
+// finishes on cheap chunks, without a shared counter (a claim from one would put an atomic round
+// trip on the producer's path). The producer lane of slot j loads the block's local chunks
+// 32 * round + j.
 //
 // Every wait is bounded (about 2 s of wall time): a wait that runs out records
 // SMCSD_ERR_TIMEOUT in the workspace and the warp leaves; the producer, before it leaves,
@@ -192,46 +193,23 @@ __device__ __noinline__ void tma_producer(const StreamParams& p, unsigned char* 
     bool done = !active;
     unsigned streak = 0;  // failed polls in a row, and when the streak began
     unsigned long long t_streak = 0;
-    // This block's shares of the two lists and their order: the precise chunks the fast list
-    // cannot pair up first (phase 0, local chunks k < E), then groups of one precise chunk and
-    // fslots fast ones (phase 1, L1 chunks), then the fast chunks left over (phase 2), so that a
-    // block's last chunks are cheap ones. The fast list is dealt in reverse block order, so that
-    // the blocks holding one precise chunk more than others hold no extra fast chunk. Each lane
-    // tracks k1 = k - E = q * m + r (m = fslots + 1) incrementally once k1 >= 0, in 32-bit
-    // arithmetic (every index is below 2^31), so a refill costs no division.
-    const uint32_t Bu = gridDim.x, bu = blockIdx.x, bf = Bu - 1u - bu, m = (uint32_t)p.fslots + 1u;
-    const uint32_t Pb = p.n_precise > (long long)bu ? (uint32_t)((p.n_precise - 1 - bu) / Bu) + 1u : 0u;
-    const uint32_t Fb = p.n_fast > (long long)bf ? (uint32_t)((p.n_fast - 1 - bf) / Bu) + 1u : 0u;
-    const uint32_t G1 = p.fslots > 0 ? min(Pb, Fb / (uint32_t)p.fslots) : 0u;
-    const uint32_t E = Pb - G1, L1 = G1 * m;
-    const uint32_t dq = kRing / m, dr = kRing % m;  // k1 += 32 moves q by dq and r by dr
-    uint32_t k = (uint32_t)slot, q = 0, r = 0;
-    if (k >= E) {
-        q = (k - E) / m;
-        r = (k - E) % m;
-    }
-    // residual pairs: block b takes pairs b, b+B, ...; local chunk k is half k & 1 of pair k >> 1
-    const uint32_t Qb = KIND == 2 && p.n_precise > (long long)bu ? (uint32_t)((p.n_precise - 1 - bu) / Bu) + 1u : 0u;
-    auto local_item = [&]() -> long long {  // tag item of local chunk k, or -1
-        if (KIND == 2) {
-            const uint32_t jp = k >> 1;
+    // This block's shares of the two lists and their order (smcsd_deal.h); lane `slot` walks
+    // local chunks slot, slot + kRing, ...
+    const uint32_t Bu = gridDim.x, bu = blockIdx.x;
+    Deal d = deal_init(KIND == 0 ? p.n_precise : 0, KIND == 0 ? p.n_fast : 0, p.fper, Bu, bu,
+                       (uint32_t)slot, kRing);
+    const uint32_t Qb = deal_share(p.n_precise, Bu, bu);  // (KIND 2: pairs; KIND 1: chunks)
+    auto local_item = [&]() -> long long {  // tag item of local chunk d.k, or -1
+        if (KIND == 2) {  // residual pairs: local chunk k is half k & 1 of pair k >> 1
+            const uint32_t jp = d.k >> 1;
             if (jp >= Qb) return -1;
-            return (long long)((((jp * Bu + bu) << 1) | (k & 1u)) | 0x80000000u);
+            return (long long)((((jp * Bu + bu) << 1) | (d.k & 1u)) | kPreciseBit);
         }
-        uint32_t j;
-        bool precise;
-        if (k < E) {
-            precise = true;
-            j = k;
-        } else if (k - E < L1) {
-            precise = r == 0;
-            j = precise ? E + q : q * (uint32_t)p.fslots + r - 1u;
-        } else {
-            precise = false;
-            j = G1 * (uint32_t)p.fslots + (k - E - L1);
-            if (j >= Fb) return -1;
+        if (KIND == 1) {  // all precise: items b, b+B, ...
+            if (d.k >= Qb) return -1;
+            return (long long)((d.k * Bu + bu) | kPreciseBit);
         }
-        return precise ? (long long)((j * Bu + bu) | 0x80000000u) : (long long)(j * Bu + bf);
+        return deal_item(d);
     };
     bool moved = true;
     while (__any_sync(0xffffffffu, !done)) {
@@ -283,18 +261,7 @@ __device__ __noinline__ void tma_producer(const StreamParams& p, unsigned char* 
         }
         tag_store(tb, round * kRing + (uint32_t)slot, (c.valid && sane) ? (uint32_t)it : 0xffffffffu);
         ++round;
-        if (k >= E) {
-            q += dq;
-            r += dr;
-            if (r >= m) {
-                r -= m;
-                ++q;
-            }
-        } else if (k + kRing >= E) {  // k1 turns non-negative: one division
-            q = (k + kRing - E) / m;
-            r = (k + kRing - E) % m;
-        }
-        k += kRing;
+        deal_advance(d, kRing);
     }
     // the copy of this lane's last chunk may still be in flight: wait for it before leaving
     if (round > 0) mbar_wait(fb, (round - 1) & 1u);
@@ -576,10 +543,11 @@ static cudaError_t launch_tma_t(const StreamParams& p0, cudaStream_t st) {
     } else {
         // the sampled rows (one per particle) form the precise list; in SD mode every row is fast
         const bool sampled = MODE != kModeSD;
-        p.fslots = sampled ? p.slots - 1 : p.slots;
+        p.fslots = sampled ? (p.drf_logq ? p.R.K : p.slots - 1) : p.slots;
         p.n_precise = sampled ? (long long)p.R.S * p.cpr : 0;
         p.n_fast = (long long)p.R.S * p.fslots * p.cpr;
         p.div_fseq = make_fastdiv((uint32_t)(p.fslots > 0 ? p.fslots * p.cpr : 1));
+        p.fper = sampled ? deal_fper(p.fslots) : p.fslots;
     }
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
