@@ -35,11 +35,13 @@ NSETS = 4
 
 
 DEFAULT_WORKLOAD = "smc_sd_step_8x16_k4_v128256_bf16"
-# name -> (kind, config); "smc": one smc_step per step, "sd": one sd_verify per step, "draft": one
+# name -> (kind, config); "smc": one smc_step per step, "smc_logq": one smc_step_logq per step
+# (the draft given as the sampler's log q), "sd": one sd_verify per step, "draft": one
 # draft_sample over the S*K draft rows per step
 WORKLOADS = {
     DEFAULT_WORKLOAD: ("smc", "SMC_LLAMA3"),
     "smc_sd_step_4x64_k8_v151936_bf16_power": ("smc", "SMC_QWEN_POWER"),
+    "smc_sd_step_logq_8x16_k4_v128256_bf16": ("smc_logq", "SMC_LLAMA3"),
     "sd_verify_128_k4_v128256_bf16": ("sd", "SMC_LLAMA3"),
     "sd_verify_16_k4_v32000_bf16": ("sd", None),
     "draft_sample_512_v128256_bf16": ("draft", "SMC_LLAMA3"),
@@ -71,9 +73,13 @@ def workload_config(name: str = DEFAULT_WORKLOAD):
                f"{NSETS} rotating logit sets of {lb / 1e6:.1f} MB; L2 flushed (256 MB "
                f"write) before every timed graph replay of {NSETS} calls"),
     }
-    if kind == "smc":
+    if kind in ("smc", "smc_logq"):
         config.update({"G": cfg.G, "N": cfg.N, "alpha": cfg.alpha,
                        "ess_threshold": cfg.ess_threshold, "ctx": cfg.ctx, "page": cfg.page})
+        if kind == "smc_logq":
+            config["draft"] = ("tokens and log q from draft_sample on the draft logits (before the "
+                               "timed region, as the draft tokens of the logits workload); the step "
+                               "reads the target logits only")
     elif kind == "draft":
         config.update({"rows": cfg.S * cfg.K, "positions": "drafted tokens (one per draft row)"})
     else:
@@ -84,6 +90,8 @@ def workload_config(name: str = DEFAULT_WORKLOAD):
 def logit_bytes(cfg, kind: str = "smc") -> int:
     if kind == "draft":  # the draft rows only
         return cfg.S * cfg.K * cfg.V * 2
+    if kind == "smc_logq":  # the target rows only
+        return cfg.S * (cfg.K + 1) * cfg.V * 2
     return cfg.S * (2 * cfg.K + 1) * cfg.V * 2
 
 
@@ -100,6 +108,8 @@ def algorithmic_bytes(cfg, kind: str = "smc") -> int:
         return logit_bytes(cfg, kind) + cfg.S * cfg.K * 12
     small = (cfg.S * cfg.K * 4 + cfg.S * 4 + cfg.G * 4 + cfg.S * 4 * 2 + cfg.S * 4 + cfg.G * 8
              + 2 * cfg.S * cfg.pages_per_seq * 4 + cfg.S * cfg.pages_per_seq * 4)
+    if kind == "smc_logq":  # plus the given log q of every draft token
+        return logit_bytes(cfg, kind) + small + cfg.S * cfg.K * 4
     return logit_bytes(cfg) + small
 
 
@@ -113,6 +123,8 @@ KERNEL_NOTE = {
     "sd": "one sd_verify call: the stream over every row, the SD epilogue, the final-token rows "
           "and residual passes with their epilogues; achieved = algorithmic bytes per call / "
           "device time per call",
+    "smc_logq": "one smc_step_logq call: stream_tma_kernel over the target rows and finish_kernel; "
+                "achieved = algorithmic bytes per step / device time per step",
     "draft": "one draft_sample call: stream_tma_kernel (precise partials of every row) and "
              "finish_kernel (one inverse-CDF draw per row); achieved = algorithmic bytes per call "
              "/ device time per call",
@@ -394,7 +406,8 @@ def run_reference(args):
 
 
 def parallelism(kind: str, world: int) -> str:
-    unit_name = {"smc": "prompt groups", "sd": "sequences", "draft": "draft rows"}.get(kind, "units")
+    unit_name = {"smc": "prompt groups", "smc_logq": "prompt groups", "sd": "sequences",
+                 "draft": "draft rows"}.get(kind, "units")
     return f"replicas x{world} (independent {unit_name} per GPU, no collective)"
 
 
@@ -651,10 +664,14 @@ def run_gpu(args):
         toks = synth.torch_gumbel_draft_tokens(77 + 1000 * rank + i, drf, cfg.temperature)
         ub = torch.from_numpy(synth.uniforms(rank, S, stream=100 + 2 * i)).to(dev)
         ur = torch.from_numpy(synth.uniforms(rank, G, stream=101 + 2 * i)).to(dev)
+        if kind == "smc_logq":  # the draft sampler's tokens and log q stand in for the draft rows
+            ud = torch.from_numpy(synth.uniforms(rank, S * K, stream=700 + i)).to(dev)
+            toks, logq = B.draft_sample(drf, S * K, V, cfg.temperature, ud)
+            drf = logq
         sets.append((tgt, drf, toks, ub, ur))
     torch.cuda.synchronize()
     ws = (B.Workspace(B.OP_DRAFT_SAMPLE, S * K, 0, V, dev) if kind == "draft" else
-          B.Workspace(B.OP_SMC_STEP if kind == "smc" else B.OP_SD_VERIFY, S, K, V, dev))
+          B.Workspace(B.OP_SMC_STEP if kind in ("smc", "smc_logq") else B.OP_SD_VERIFY, S, K, V, dev))
     draft_out = (torch.empty(S * K, dtype=torch.int32, device=dev),
                  torch.empty(S * K, dtype=torch.float32, device=dev))
     usd = [torch.from_numpy(synth.uniforms(rank, S * (K + 1), stream=300 + i)).to(dev)
@@ -680,6 +697,12 @@ def run_gpu(args):
         if kind == "draft":
             B.draft_sample(drf, S * K, V, cfg.temperature, usd[i % NSETS][:S * K], ws=ws,
                            tokens=draft_out[0], logq=draft_out[1], stream=stream)
+            return
+        if kind == "smc_logq":  # (drf holds log q here)
+            B.smc_step_logq(tgt, toks, drf, G, N, K, V, cfg.temperature, cfg.alpha, ub, logw,
+                            cfg.ess_threshold, ur, table_in=tables[i % 2], pages_per_seq=P,
+                            num_pages=S * P, ws=ws, table_out=tables[(i + 1) % 2], stream=stream,
+                            **outs)
             return
         B.smc_step(tgt, drf, toks, G, N, K, V, cfg.temperature, cfg.alpha, ub, logw,
                    cfg.ess_threshold, ur, table_in=tables[i % 2], pages_per_seq=P,

@@ -260,6 +260,28 @@ int smc_step(const void* tgt_logits, const void* drf_logits, int dtype,
              void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * smc_step with the draft's log-probabilities in place of its logits ([SMC] sec. 2 steps 1 and 3:
+ * the draft proposes each token from its own distribution, and the weight needs only the
+ * probability the draft gave the proposed token). drf_logq: float [G*N*K], log q_k(x_k) of draft
+ * token draft_tokens[s*K+k] under the draft's tempered distribution at `temperature`, as
+ * draft_sample returns it when it draws the tokens. The step then reads only the target logits
+ * (target [G*N*(K+1), V]); its results are those of smc_step on draft logits whose normalised
+ * log-probabilities at the draft tokens equal drf_logq:
+ *   logw[s] += sum_{k<K} ( log pi_k(x_k) - drf_logq[s*K+k] ),
+ * with pi = softmax(alpha z_t / T), then the bonus token, ESS, resampling and remap as smc_step.
+ * The values of drf_logq are taken as given (non-positive and finite for a real distribution; a
+ * NaN makes the particle's weight NaN, reported as SMCSD_ERR_NONFINITE by the group's ESS).
+ * Arguments otherwise as smc_step; ws: smcsd_workspace_size(SMCSD_OP_SMC_STEP, G*N, K, V).
+ */
+int smc_step_logq(const void* tgt_logits, int dtype, const int32_t* draft_tokens,
+                  const float* drf_logq, int G, int N, int K, int V, float temperature, float alpha,
+                  const float* bonus_uniforms, float* logw, int32_t* bonus_token,
+                  float ess_threshold, const float* resample_uniforms, int32_t* ancestors,
+                  float* ess, int32_t* resampled, const int32_t* table_in, int32_t* table_out,
+                  int pages_per_seq, int32_t* refcount, int num_pages, void* ws, size_t ws_bytes,
+                  void* stream);
+
+/*
  * smc_step toward a tilted target: target, log_reward and reward_scale as in
  * smc_reweight_tilted; everything else as in smc_step. The reward enters the log-weights
  * before the group's ESS and resampling.

@@ -55,6 +55,8 @@ def load(path: str = LIB_PATH):
                              P, sz, P]
     lib.smc_step_static.argtypes = [P, P, i, P, i, i, i, i, f, f, P, P, P, f, P, P, P, P, P, P, i,
                                     P, i, P, P]
+    lib.smc_step_logq.argtypes = [P, i, P, P, i, i, i, i, f, f, P, P, P, f, P, P, P, P, P, P, i, P,
+                                  i, P, sz, P]
     lib.smc_reweight_tilted.argtypes = [P, P, i, P, i, i, i, f, f, i, P, f, P, P, P, P, P, P, sz, P]
     lib.smc_step_tilted.argtypes = [P, P, i, P, i, i, i, i, f, f, i, P, f, P, P, P, f, P, P, P, P,
                                     P, P, i, P, i, P, sz, P]
@@ -63,7 +65,7 @@ def load(path: str = LIB_PATH):
     lib.smcsd_selftest_wait.argtypes = [ctypes.c_uint, P, sz, P]
     for fn in ("smcsd_workspace_init", "smcsd_check_status", "sd_verify", "smc_reweight",
                "smc_ess_resample", "kv_pagetable_remap", "pacer_block_stop", "smc_step",
-               "smc_step_static", "smc_reweight_tilted", "smc_step_tilted",
+               "smc_step_static", "smc_step_logq", "smc_reweight_tilted", "smc_step_tilted",
                "pacer_block_stop_pos", "draft_sample", "smcsd_selftest_wait"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
@@ -339,6 +341,37 @@ def smc_step(tgt_logits, drf_logits, draft_tokens, G, N, K, V, temperature, alph
                          _ptr(table_in), _ptr(table_out), pages_per_seq, _ptr(refcount), num_pages,
                          w, n, _stream(stream))
     _check(rc, "smc_step")
+    return dict(bonus_token=bonus_token, ancestors=ancestors, ess=ess, resampled=resampled,
+                table_out=table_out, refcount=refcount)
+
+
+def smc_step_logq(tgt_logits, draft_tokens, drf_logq, G, N, K, V, temperature, alpha,
+                  bonus_uniforms, logw, ess_threshold, resample_uniforms, table_in=None,
+                  pages_per_seq=0, num_pages=0, ws=None, bonus_token=None, ancestors=None,
+                  ess=None, resampled=None, table_out=None, refcount=None, with_refcount=True,
+                  stream=None):
+    """smc_step with the draft's log q(x_k) (float32 [G*N*K]) in place of the draft logits."""
+    dev = tgt_logits.device
+    S = G * N
+    ws = ws or Workspace(OP_SMC_STEP, S, K, V, dev)
+    bonus_token = _out(bonus_token, (S,), torch.int32, dev)
+    ancestors = _out(ancestors, (S,), torch.int32, dev)
+    ess = _out(ess, (G,), torch.float32, dev)
+    resampled = _out(resampled, (G,), torch.int32, dev)
+    if table_in is not None:
+        table_out = _out(table_out, table_in.shape, torch.int32, dev)
+        if with_refcount and refcount is None:
+            refcount = torch.empty(num_pages, dtype=torch.int32, device=dev)
+    else:
+        table_out = refcount = None
+    w, n = ws.args
+    rc = load().smc_step_logq(_ptr(tgt_logits), _dtype_code(tgt_logits), _ptr(draft_tokens),
+                              _ptr(drf_logq), G, N, K, V, float(temperature), float(alpha),
+                              _ptr(bonus_uniforms), _ptr(logw), _ptr(bonus_token),
+                              float(ess_threshold), _ptr(resample_uniforms), _ptr(ancestors),
+                              _ptr(ess), _ptr(resampled), _ptr(table_in), _ptr(table_out),
+                              pages_per_seq, _ptr(refcount), num_pages, w, n, _stream(stream))
+    _check(rc, "smc_step_logq")
     return dict(bonus_token=bonus_token, ancestors=ancestors, ess=ess, resampled=resampled,
                 table_out=table_out, refcount=refcount)
 

@@ -155,18 +155,21 @@ static int smc_common(const void* tgt_logits, const void* drf_logits, int dtype,
                       const int32_t* draft_tokens, int S, int K, int V, float temperature,
                       float alpha, int target, const float* log_reward, float reward_scale,
                       const float* uniforms, float* logw, int32_t* bonus_token,
-                      void* ws, size_t ws_bytes, StreamParams& p) {
+                      void* ws, size_t ws_bytes, StreamParams& p,
+                      const float* drf_logq = nullptr) {
     if (dtype != SMCSD_F32 && dtype != SMCSD_BF16) return SMCSD_ERR_DTYPE;
     if (!tgt_logits || !uniforms || !bonus_token) return SMCSD_ERR_INVALID_ARG;
     if (S <= 0 || K < 0 || V <= 0) return SMCSD_ERR_INVALID_ARG;
     if (!finite_pos(temperature) || !finite_pos(alpha)) return SMCSD_ERR_INVALID_ARG;
     if (target != SMCSD_TARGET_TOKEN && target != SMCSD_TARGET_SEQUENCE) return SMCSD_ERR_INVALID_ARG;
     if (log_reward && !isfinite(reward_scale)) return SMCSD_ERR_INVALID_ARG;
-    if (K > 0 && (!drf_logits || !draft_tokens)) return SMCSD_ERR_INVALID_ARG;
+    if (K > 0 && ((!drf_logits && !drf_logq) || !draft_tokens)) return SMCSD_ERR_INVALID_ARG;
     const WsLayout L = ws_layout(S, K, V);
     int rc = check_ws(ws, ws_bytes, L.total);
     if (rc) return rc;
+    if (drf_logq) drf_logits = nullptr;  // the draft rows are not read
     p.R = Rows{tgt_logits, drf_logits, draft_tokens, nullptr, nullptr, S, K, V};
+    p.drf_logq = K > 0 ? drf_logq : nullptr;
     p.dtype = dtype;
     p.vec = aligned16(tgt_logits) && (K == 0 || aligned16(drf_logits)) &&
             ((size_t)V * elem_bytes(dtype)) % 16 == 0;
@@ -225,16 +228,15 @@ extern "C" int smc_reweight(const void* tgt_logits, const void* drf_logits, int 
                                bonus_token, lse_tgt, lse_drf, ws, ws_bytes, stream);
 }
 
-extern "C" int smc_step_tilted(const void* tgt_logits, const void* drf_logits, int dtype,
-                               const int32_t* draft_tokens, int G, int N, int K, int V,
-                               float temperature, float alpha, int target,
-                               const float* log_reward, float reward_scale,
-                               const float* bonus_uniforms, float* logw, int32_t* bonus_token,
-                               float ess_threshold, const float* resample_uniforms,
-                               int32_t* ancestors, float* ess, int32_t* resampled,
-                               const int32_t* table_in, int32_t* table_out, int pages_per_seq,
-                               int32_t* refcount, int num_pages, void* ws, size_t ws_bytes,
-                               void* stream) {
+static int smc_step_impl(const void* tgt_logits, const void* drf_logits, const float* drf_logq,
+                         int dtype, const int32_t* draft_tokens, int G, int N, int K, int V,
+                         float temperature, float alpha, int target, const float* log_reward,
+                         float reward_scale, const float* bonus_uniforms, float* logw,
+                         int32_t* bonus_token, float ess_threshold, const float* resample_uniforms,
+                         int32_t* ancestors, float* ess, int32_t* resampled,
+                         const int32_t* table_in, int32_t* table_out, int pages_per_seq,
+                         int32_t* refcount, int num_pages, void* ws, size_t ws_bytes,
+                         void* stream) {
     if (G <= 0 || N <= 0 || (long long)G * N > 0x7fffffffLL) return SMCSD_ERR_INVALID_ARG;
     if (!logw || !resample_uniforms || !ancestors || isnan(ess_threshold)) return SMCSD_ERR_INVALID_ARG;
     const bool remap = table_in != nullptr;
@@ -247,7 +249,7 @@ extern "C" int smc_step_tilted(const void* tgt_logits, const void* drf_logits, i
     StreamParams p{};
     int rc = smc_common(tgt_logits, drf_logits, dtype, draft_tokens, G * N, K, V, temperature,
                         alpha, target, log_reward, reward_scale, bonus_uniforms, logw,
-                        bonus_token, ws, ws_bytes, p);
+                        bonus_token, ws, ws_bytes, p, drf_logq);
     if (rc) return rc;
     cudaStream_t st = (cudaStream_t)stream;
     p.mode = kModeSMCStep;
@@ -264,6 +266,39 @@ extern "C" int smc_step_tilted(const void* tgt_logits, const void* drf_logits, i
     p.refcount = remap ? refcount : nullptr;  // zeroed by the streaming pass
     p.num_pages = num_pages;
     return from_cuda(launch_stream(p, st));
+}
+
+extern "C" int smc_step_tilted(const void* tgt_logits, const void* drf_logits, int dtype,
+                               const int32_t* draft_tokens, int G, int N, int K, int V,
+                               float temperature, float alpha, int target,
+                               const float* log_reward, float reward_scale,
+                               const float* bonus_uniforms, float* logw, int32_t* bonus_token,
+                               float ess_threshold, const float* resample_uniforms,
+                               int32_t* ancestors, float* ess, int32_t* resampled,
+                               const int32_t* table_in, int32_t* table_out, int pages_per_seq,
+                               int32_t* refcount, int num_pages, void* ws, size_t ws_bytes,
+                               void* stream) {
+    return smc_step_impl(tgt_logits, drf_logits, nullptr, dtype, draft_tokens, G, N, K, V,
+                         temperature, alpha, target, log_reward, reward_scale, bonus_uniforms,
+                         logw, bonus_token, ess_threshold, resample_uniforms, ancestors, ess,
+                         resampled, table_in, table_out, pages_per_seq, refcount, num_pages, ws,
+                         ws_bytes, stream);
+}
+
+extern "C" int smc_step_logq(const void* tgt_logits, int dtype, const int32_t* draft_tokens,
+                             const float* drf_logq, int G, int N, int K, int V, float temperature,
+                             float alpha, const float* bonus_uniforms, float* logw,
+                             int32_t* bonus_token, float ess_threshold,
+                             const float* resample_uniforms, int32_t* ancestors, float* ess,
+                             int32_t* resampled, const int32_t* table_in, int32_t* table_out,
+                             int pages_per_seq, int32_t* refcount, int num_pages, void* ws,
+                             size_t ws_bytes, void* stream) {
+    if (K > 0 && !drf_logq) return SMCSD_ERR_INVALID_ARG;
+    return smc_step_impl(tgt_logits, nullptr, drf_logq, dtype, draft_tokens, G, N, K, V,
+                         temperature, alpha, SMCSD_TARGET_TOKEN, nullptr, 0.0f, bonus_uniforms,
+                         logw, bonus_token, ess_threshold, resample_uniforms, ancestors, ess,
+                         resampled, table_in, table_out, pages_per_seq, refcount, num_pages, ws,
+                         ws_bytes, stream);
 }
 
 extern "C" int smc_step(const void* tgt_logits, const void* drf_logits, int dtype,

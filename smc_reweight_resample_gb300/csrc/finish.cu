@@ -87,7 +87,9 @@ __global__ void __launch_bounds__(kFinishMaxWarps * kWarp)
     griddep_wait();
     if (ks < 0) return;  // (the same on every thread of the block)
     const PreciseCtx P{p.sc_t, &sT, nullptr, p.ws, p.direct};
-    for (int slot = warp; slot <= 2 * ks; slot += nw) row_epilogue<DT, MODE>(p, P, s, slot, ks, lane, sL);
+    for (int slot = warp; slot <= 2 * ks; slot += nw)
+        if (!(p.drf_logq && slot < 2 * ks && (slot & 1)))  // (draft rows with a given log q)
+            row_epilogue<DT, MODE>(p, P, s, slot, ks, lane, sL);
     // The sequence (and group) epilogue needs only the rows with a draft token. When the block has
     // a warp per row, the bonus row's warp (warp 2ks) keeps drawing while the others go on, meeting
     // at a named barrier without it; otherwise the whole block meets.

@@ -28,6 +28,44 @@ __device__ __forceinline__ void load_exp2_table(const Exp2Table& src, Exp2Table&
     __syncthreads();
 }
 
+// The (K+1)-th token of particle s, drawn by inverse CDF from pi at target row ks with the row's
+// precise partials (warp-wide; stores the token, the row's normaliser and the log-probability of
+// the token where asked). Returns, on lane 0, the token's weight factor under the whole-sequence
+// power target ((alpha - 1) log p(b) as a double-float; zero otherwise).
+template <int DT>
+__device__ __forceinline__ float2 bonus_draw(const StreamParams& p, const PreciseCtx& P, int s, int ks,
+                                             int lane) {
+    const Rows& R = p.R;
+    const float4* tot = ws_ptr<float4>(p.ws, p.L.ddtot) + (size_t)(s * 2) * p.cpr;
+    const float4* sub = ws_ptr<float4>(p.ws, p.L.ddsub) + (size_t)(s * 2) * p.cpr * kSubs;
+    const long long row = trow_of(R, s, ks);
+    float lse = 0.0f;
+    const int tok = draw_precise_row<DT>(tot, sub, p.cpr, row_ptr<DT>(R.tgt, row, R.V), R.V, P,
+                                         __ldg(p.uniforms + s), lane, &lse);
+    float2 fac = make_float2(0.0f, 0.0f);
+    if (lane == 0) {
+        if (tok < 0) raise_error(p.ws, kErrNonfinite);
+        p.bonus_token[s] = tok < 0 ? 0 : tok;
+        if (p.lse_tgt) p.lse_tgt[row] = lse;
+        if (p.target_seq || p.bonus_logq) {
+            // log-probability of the drawn token, c z_tok - lse
+            dd lp{0.0f, 0.0f};
+            if (tok >= 0) {
+                const float z = logit_at<DT>(row_ptr<DT>(R.tgt, row, R.V), tok);
+                lp = dd_sub(dd_mul_f(dd{p.sc_t.c_hi, p.sc_t.c_lo}, z), dd{lse, 0.0f});
+            }
+            if (p.bonus_logq) p.bonus_logq[s] = f_add(lp.hi, lp.lo);
+            if (p.target_seq && p.alpha != 1.0f) {
+                // whole-sequence power target: the (K+1)-th token, drawn from p, carries the
+                // weight factor p^(alpha-1), i.e. (alpha - 1) lp in log space
+                const dd inc = dd_mul(lp, two_sum(p.alpha, -1.0f));  // exact alpha - 1
+                fac = make_float2(inc.hi, inc.lo);
+            }
+        }
+    }
+    return fac;
+}
+
 // One row: the row's normaliser (into sL[slot], and the optional lse outputs), or, for the bonus
 // row of a particle, the (K+1)-th token drawn from pi with the row's normaliser as a by-product.
 template <int DT, int MODE>
@@ -36,33 +74,8 @@ __device__ __noinline__ void row_epilogue(const StreamParams& p, const PreciseCt
     const Rows& R = p.R;
     const int k = slot >> 1;
     if (MODE != kModeSD && slot == 2 * ks) {
-        const float4* tot = ws_ptr<float4>(p.ws, p.L.ddtot) + (size_t)(s * 2) * p.cpr;
-        const float4* sub = ws_ptr<float4>(p.ws, p.L.ddsub) + (size_t)(s * 2) * p.cpr * kSubs;
-        const long long row = trow_of(R, s, ks);
-        float lse = 0.0f;
-        const int tok = draw_precise_row<DT>(tot, sub, p.cpr, row_ptr<DT>(R.tgt, row, R.V), R.V, P,
-                                             __ldg(p.uniforms + s), lane, &lse);
-        if (lane == 0) {
-            if (tok < 0) raise_error(p.ws, kErrNonfinite);
-            p.bonus_token[s] = tok < 0 ? 0 : tok;
-            if (p.lse_tgt) p.lse_tgt[row] = lse;
-            if (p.target_seq || p.bonus_logq) {
-                // log-probability of the drawn token, c z_tok - lse
-                dd lp{0.0f, 0.0f};
-                if (tok >= 0) {
-                    const float z = logit_at<DT>(row_ptr<DT>(R.tgt, row, R.V), tok);
-                    lp = dd_sub(dd_mul_f(dd{p.sc_t.c_hi, p.sc_t.c_lo}, z), dd{lse, 0.0f});
-                }
-                if (p.bonus_logq) p.bonus_logq[s] = f_add(lp.hi, lp.lo);
-                if (p.target_seq) {
-                    // whole-sequence power target: the (K+1)-th token, drawn from p, carries
-                    // the weight factor p^(alpha-1), i.e. (alpha - 1) lp in log space
-                    const dd inc = p.alpha != 1.0f ? dd_mul(lp, two_sum(p.alpha, -1.0f))  // exact alpha - 1
-                                                   : dd{0.0f, 0.0f};
-                    sL[slot] = make_float2(inc.hi, inc.lo);
-                }
-            }
-        }
+        const float2 fac = bonus_draw<DT>(p, P, s, ks, lane);
+        if (lane == 0 && p.target_seq) sL[slot] = fac;
         return;
     }
     const bool is_draft = slot < 2 * ks && (slot & 1);
@@ -91,7 +104,9 @@ __device__ __forceinline__ void prefetch_token_logit(const StreamParams& p, int 
     const bool is_draft = slot & 1;
     const int x = __ldg(R.toks + drow_of(R, s, k));
     float z = 0.0f;
-    if (x >= 0 && x < R.V)
+    if (is_draft && p.drf_logq)
+        z = __ldg(p.drf_logq + drow_of(R, s, k));  // (draft slots then hold log q itself)
+    else if (x >= 0 && x < R.V)
         z = is_draft ? logit_at<DT>(row_ptr<DT>(R.drf, drow_of(R, s, k), R.V), x)
                      : logit_at<DT>(row_ptr<DT>(R.tgt, trow_of(R, s, k), R.V), x);
     sX[slot] = x;
@@ -109,9 +124,14 @@ __device__ __forceinline__ bool log_probs(const StreamParams& p, int k, const fl
         raise_error(p.ws, kErrRange);
         return false;
     }
-    const float2 Lt = sL[2 * k], Ld = sL[2 * k + 1];
+    const float2 Lt = sL[2 * k];
     lt = dd_sub(dd_mul_f(dd{p.sc_t.c_hi, p.sc_t.c_lo}, sZ[2 * k]), dd{Lt.x, Lt.y});
-    ld = dd_sub(dd_mul_f(dd{p.sc_d.c_hi, p.sc_d.c_lo}, sZ[2 * k + 1]), dd{Ld.x, Ld.y});
+    if (p.drf_logq) {
+        ld = dd{sZ[2 * k + 1], 0.0f};  // the given log q_k(x_k)
+    } else {
+        const float2 Ld = sL[2 * k + 1];
+        ld = dd_sub(dd_mul_f(dd{p.sc_d.c_hi, p.sc_d.c_lo}, sZ[2 * k + 1]), dd{Ld.x, Ld.y});
+    }
     return true;
 }
 
@@ -247,6 +267,7 @@ __device__ __forceinline__ ChunkRef chunk_ref_two_list(const StreamParams& p, ui
         const uint32_t rem = tag_item - (uint32_t)c.s * p.div_fseq.d;
         c.slot = (int)fast_div(rem, p.div_cpr);
         c.chunk = (int)(rem - (uint32_t)c.slot * p.div_cpr.d);
+        if (p.drf_logq) c.slot *= 2;  // fast rows are the target rows 0 .. K-1 only
         c.ks = seq_len(p.R, c.s, p.ws);
     }
     c.valid = c.ks >= 0 && c.slot <= 2 * c.ks;
@@ -376,7 +397,7 @@ __device__ __forceinline__ ChunkRef chunk_ref(const StreamParams& p, uint32_t it
     c.chunk = (int)(rem - (uint32_t)pos * p.div_cpr.d);
     c.ks = seq_len(p.R, c.s, p.ws);
     c.slot = pos == 0 ? 2 * c.ks : pos - 1;
-    c.valid = c.ks >= 0 && pos <= 2 * c.ks;
+    c.valid = c.ks >= 0 && pos <= 2 * c.ks && !(p.drf_logq && pos > 0 && (c.slot & 1));
     c.is_draft = c.slot < 2 * c.ks && (c.slot & 1);
     const int k = c.slot >> 1;
     c.row = c.valid ? (c.is_draft ? drow_of(p.R, c.s, k) : trow_of(p.R, c.s, k)) : 0;
