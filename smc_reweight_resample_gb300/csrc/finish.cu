@@ -26,7 +26,7 @@ constexpr int kFinishMaxWarps = 16;
 // stand-alone resampling and page-table kernels after this pass: their code kept out of this
 // kernel, whose every SM runs it cold, keeps its instruction footprint small.
 __device__ __forceinline__ void group_part(const StreamParams& p, int g, int32_t* sAnc, int* sRes,
-                                           int bar, int nthr) {
+                                           int bar, int nthr, const Exp2Table& T) {
     const int N = p.N;
     const int lane = threadIdx.x & 31;
     int32_t* anc = p.ancestors + (size_t)g * N;
@@ -36,7 +36,7 @@ __device__ __forceinline__ void group_part(const StreamParams& p, int g, int32_t
         int32_t* rs = p.resampled ? p.resampled + g : nullptr;
         const float U = __ldg(p.resample_uniforms + g);
         int a[1];
-        const bool res = group_resample_small<1>(lw, N, p.ess_threshold, U, anc, ess, rs, p.ws, lane, p.T, a);
+        const bool res = group_resample_small<1>(lw, N, p.ess_threshold, U, anc, ess, rs, p.ws, lane, T, a);
         if (lane < N) sAnc[lane] = a[0];
         if (lane == 0) *sRes = res ? 1 : 0;
     }
@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(kFinishMaxWarps * kWarp)
     bar_sync(bar, nthr);
     if (warp == 0) {
         if (MODE == kModeSD) {
-            sd_seq_epilogue(p, s, ks, lane, sL, sX, sZ);
+            sd_seq_epilogue(p, s, ks, lane, sL, sX, sZ, sT);
         } else {
             smc_particle_epilogue(p, s, lane, __shfl_sync(0xffffffffu, lw_old, 0), sL, sX, sZ);
             if (MODE == kModeSMCStep && p.N <= kWarp) {
@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(kFinishMaxWarps * kWarp)
     }
     if (MODE != kModeSMCStep || p.N > kWarp) return;
     bar_sync(bar, nthr);
-    if (sLast) group_part(p, s / p.N, sAnc, &sRes, bar, nthr);
+    if (sLast) group_part(p, s / p.N, sAnc, &sRes, bar, nthr, sT);  // (the block's shared copy)
 }
 
 static cudaError_t launch_dependent(const void* kern, dim3 grid, dim3 block, size_t smem,

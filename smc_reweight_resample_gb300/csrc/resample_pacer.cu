@@ -12,13 +12,20 @@
 namespace smcsd {
 
 __global__ void __launch_bounds__(128) resample_kernel(const __grid_constant__ ResampleParams p) {
+    // the exp table in shared memory: lanes index it at different entries
+    __shared__ Exp2Table sT;
+    for (int i = threadIdx.x; i < 32; i += blockDim.x) {
+        sT.hi[i] = p.T.hi[i];
+        sT.lo[i] = p.T.lo[i];
+    }
+    __syncthreads();
     const int lane = threadIdx.x & 31;
     const int g = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (g >= p.G) return;
     const size_t o = (size_t)g * p.N;
     group_resample(p.logw + o, p.N, p.ess_threshold, __ldg(p.uniforms + g), p.ancestors + o,
                    p.ess ? p.ess + g : nullptr, p.resampled ? p.resampled + g : nullptr, p.ws, lane,
-                   p.T);
+                   sT);
 }
 
 __global__ void __launch_bounds__(256) remap_kernel(const __grid_constant__ RemapParams p) {

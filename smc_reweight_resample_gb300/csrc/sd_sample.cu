@@ -3,13 +3,23 @@
 // acceptance length, draw either the bonus token from p at the last target row, or the
 // correction token from normalise(max(0, p - q)) at the rejected position, by inverse CDF.
 //
-// Pass 2 (sd_rows_kernel): double-float chunk sums of exp(z/T) over the row(s) to draw from.
-//   Its per-sequence epilogue draws the bonus token directly, or turns the sums into the
-//   reciprocal normalisers 1/Z_t, 1/Z_d that the residual needs.
-// Pass 3 (sd_residual_kernel): double-float sums of max(0, p_i - q_i) per lane block; its
-//   epilogue draws the correction token (or falls back to p at the same row if the residual
-//   has no mass).
-// Both passes re-read one or two rows per sequence, which the first pass has just streamed.
+// Rows 16-byte aligned (the common case): one more pipelined pass (stream_tma.cu, kModeSDFinal)
+// over the (target, draft) row pair each sequence draws from gives the precise partials of a
+// bonus row, or, for a rejected position, per lane block the double-float sums of exp(c z_t) and
+// exp(c z_d) over all positions (the two normalisers) and over the positions with
+// z_t - z_d > theta = (L_t - L_d) / c, which are exactly those with p_i > q_i up to the float
+// accuracy of theta (a position that close to the boundary has a residual of at most ~1e-6 of its
+// p_i). sd_final_finish_kernel then draws: the residual's chunk and lane-block masses are
+// A / Z_t - B / Z_d, and the one lane block it rescans takes max(0, p_i - q_i) position by
+// position.
+// Rows not aligned: the direct-load passes below. Pass 2 (sd_rows_kernel): double-float chunk
+// sums of exp(z/T) over the row(s) to draw from; its per-sequence epilogue draws the bonus token
+// directly, or turns the sums into the reciprocal normalisers 1/Z_t, 1/Z_d that the residual
+// needs. Pass 3 (sd_residual_kernel): double-float sums of max(0, p_i - q_i) per lane block; its
+// epilogue draws the correction token (or falls back to p at the same row if the residual has no
+// mass).
+// The final-token passes re-read one or two rows per sequence, which the first pass has just
+// streamed.
 #include "smcsd_epilogue.cuh"
 
 namespace smcsd {
@@ -119,20 +129,6 @@ __global__ void __launch_bounds__(kSampleThreads, 3) sd_rows_kernel(const __grid
     }
 }
 
-// The per-sequence epilogue of the rows pass when that pass ran as a pipelined stream: one warp
-// per sequence, a programmatic dependent of the stream (it waits for it before reading).
-template <int DT>
-__global__ void __launch_bounds__(256) sd_rows_finish_kernel(const __grid_constant__ SampleParams p) {
-    __shared__ Exp2Table sT;
-    load_exp2_table_s(p.T, sT);
-    const PreciseCtx P{p.sc, &sT, nullptr, p.ws, p.direct};
-    const int lane = threadIdx.x & 31;
-    const int s = (int)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    griddep_wait();
-    if (s >= p.R.S || seq_len(p.R, s, p.ws) < 0) return;
-    sd_rows_epilogue<DT>(p, P, s, __ldcg(&ws_ptr<SeqState>(p.ws, p.L.seq)[s].mode), lane);
-}
-
 template <int DT>
 __device__ __noinline__ void sd_residual_epilogue(const SampleParams& p, const PreciseCtx& P,
                                                   const ResidualCtx& c, int s, const void* trp,
@@ -156,25 +152,6 @@ __device__ __noinline__ void sd_residual_epilogue(const SampleParams& p, const P
         if (tok < 0) raise_error(p.ws, kErrNonfinite);
         p.out_token[s] = tok < 0 ? 0 : tok;
     }
-}
-
-// The per-sequence residual draw when the residual pass ran as a pipelined stream: one warp per
-// sequence that draws a correction token, a programmatic dependent of the stream.
-template <int DT>
-__global__ void __launch_bounds__(256) sd_residual_finish_kernel(const __grid_constant__ SampleParams p) {
-    __shared__ Exp2Table sT;
-    load_exp2_table_s(p.T, sT);
-    const PreciseCtx P{p.sc, &sT, nullptr, p.ws, p.direct};
-    const int lane = threadIdx.x & 31;
-    const int s = (int)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    griddep_wait();
-    if (s >= p.R.S || seq_len(p.R, s, p.ws) < 0) return;
-    const SeqState* seq = ws_ptr<SeqState>(p.ws, p.L.seq);
-    if (__ldcg(&seq[s].mode) != 1) return;
-    const ResidualCtx c = residual_ctx(seq + s, P);
-    const void* trp = row_ptr<DT>(p.R.tgt, __ldcg(&seq[s].trow), p.R.V);
-    const void* drp = row_ptr<DT>(p.R.drf, __ldcg(&seq[s].drow), p.R.V);
-    sd_residual_epilogue<DT>(p, P, c, s, trp, drp, lane);
 }
 
 template <int DT>
@@ -254,6 +231,135 @@ __global__ void __launch_bounds__(kSampleThreads, 3)
     }
 }
 
+// Chunk and lane-block records of the residual max(0, p - q) of a sequence from the final-token
+// pass's sums (see final_consumer): for a chunk, (A 2^n_t a - B 2^n_d b) with a = 1/Z_t in units
+// of 2^-N_t and b = 1/Z_d in units of 2^-N_d, clamped at 0 (a position whose difference lies
+// within rounding of theta can leave a tiny negative amount), as absolute values (exponent 0).
+struct ResidualParts {
+    const float4* tot_t;  // S_t chunk totals (with n_t), then S_d's at + cpr
+    const float4* sub_t;  // {S_t, A} lane blocks; {S_d, B} at + cpr * kSubs
+    const float4* ab;     // {A, B} chunk totals
+    int cpr, Nt, Nd;
+    dd a, b;
+    __device__ __forceinline__ dd value(float ahi, float alo, float bhi, float blo, int c) const {
+        const int nt = __float_as_int(ld_cg4(tot_t + c).z), nd = __float_as_int(ld_cg4(tot_t + cpr + c).z);
+        dd x{0.0f, 0.0f}, y{0.0f, 0.0f};
+        if (nt != kNoMass && ahi > 0.0f) {
+            const float sc = pow2i(nt - Nt);
+            x = dd_mul(dd{f_mul(ahi, sc), f_mul(alo, sc)}, a);
+        }
+        if (nd != kNoMass && bhi > 0.0f) {
+            const float sc = pow2i(nd - Nd);
+            y = dd_mul(dd{f_mul(bhi, sc), f_mul(blo, sc)}, b);
+        }
+        const dd r = dd_sub(x, y);
+        return r.hi > 0.0f ? r : dd{0.0f, 0.0f};
+    }
+    __device__ __forceinline__ float4 chunk(int c) const {
+        const float4 v = ld_cg4(ab + c);
+        return pack_part(value(v.x, v.y, v.z, v.w, c), 0);
+    }
+    __device__ __forceinline__ float4 block(int c, int l) const {
+        const float4 t = ld_cg4(sub_t + (size_t)c * kSubs + l);
+        const float4 d = ld_cg4(sub_t + (size_t)(cpr + c) * kSubs + l);
+        return pack_part(value(t.z, t.w, d.z, d.w, c), 0);
+    }
+};
+
+// The target row's own partials from the same records (the zero-mass fallback: a draw from p).
+struct TargetParts {
+    const float4* tot_t;
+    const float4* sub_t;
+    __device__ __forceinline__ float4 chunk(int c) const { return ld_cg4(tot_t + c); }
+    __device__ __forceinline__ float4 block(int c, int l) const {
+        const float4 v = ld_cg4(sub_t + (size_t)c * kSubs + l);
+        return make_float4(v.x, v.y, ld_cg4(tot_t + c).z, 0.0f);
+    }
+};
+
+// The final token of each sequence after the merged final-token pass, one warp per sequence (a
+// programmatic dependent of the pass): the bonus draw from p at the last target row, or the
+// correction draw from normalise(max(0, p - q)) at the rejected position, whose normalisers and
+// residual masses come from the pass's sums; a residual without mass falls back to p.
+template <int DT>
+__global__ void __launch_bounds__(kWarp) sd_final_finish_kernel(const __grid_constant__ SampleParams p) {
+    __shared__ Exp2Table sT;
+    load_exp2_table_s(p.T, sT);
+    const PreciseCtx P{p.sc, &sT, nullptr, p.ws, p.direct};
+    const int lane = threadIdx.x & 31;
+    const int s = (int)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    griddep_wait();
+    if (s >= p.R.S || seq_len(p.R, s, p.ws) < 0) return;
+    const int cpr = p.cpr;
+    const SeqState* st = ws_ptr<SeqState>(p.ws, p.L.seq) + s;
+    const int mode = __ldcg(&st->mode);
+    const float4* tot_t = ws_ptr<float4>(p.ws, p.L.ddtot) + (size_t)(s * 2) * cpr;
+    const float4* sub_t = ws_ptr<float4>(p.ws, p.L.ddsub) + (size_t)(s * 2) * cpr * kSubs;
+    const void* trp = row_ptr<DT>(p.R.tgt, __ldcg(&st->trow), p.R.V);
+    const float u = __ldg(p.uniforms + (size_t)s * (p.R.K + 1) + p.R.K);
+    int tok;
+    if (mode == 0) {
+        tok = draw_precise_row<DT>(tot_t, sub_t, cpr, trp, p.R.V, P, u, lane, nullptr);
+    } else {
+        const void* drp = row_ptr<DT>(p.R.drf, __ldcg(&st->drow), p.R.V);
+        // both rows' common exponents and totals from one read of their chunk totals
+        int Nt = kNoMass, Nd = kNoMass;
+        dd Zt{0.0f, 0.0f}, Zd{0.0f, 0.0f};
+        if (cpr <= kDrawCache * kWarp) {
+            float4 vt[kDrawCache], vd[kDrawCache];
+#pragma unroll
+            for (int q = 0; q < kDrawCache; ++q) {
+                const int ch = lane + q * kWarp;
+                vt[q] = ch < cpr ? ld_cg4(tot_t + ch) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                vd[q] = ch < cpr ? ld_cg4(tot_t + cpr + ch) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                if (vt[q].x > 0.0f) Nt = max(Nt, __float_as_int(vt[q].z));
+                if (vd[q].x > 0.0f) Nd = max(Nd, __float_as_int(vd[q].z));
+            }
+            Nt = warp_max_i(Nt);
+            Nd = warp_max_i(Nd);
+#pragma unroll
+            for (int q = 0; q < kDrawCache; ++q) {
+                Zt = dd_add(Zt, part_value(vt[q], Nt));
+                Zd = dd_add(Zd, part_value(vd[q], Nd));
+            }
+            Zt = warp_sum_dd(Zt);
+            Zd = warp_sum_dd(Zd);
+        } else {
+            Nt = row_exponent(tot_t, cpr, lane);
+            Nd = row_exponent(tot_t + cpr, cpr, lane);
+            Zt = row_total(tot_t, cpr, Nt, lane);
+            Zd = row_total(tot_t + cpr, cpr, Nd, lane);
+        }
+        if (Nt == kNoMass || Nd == kNoMass || !(Zt.hi > 0.0f) || !(Zd.hi > 0.0f)) {
+            if (lane == 0) raise_error(p.ws, kErrNonfinite);
+            if (lane == 0) p.out_token[s] = 0;
+            return;
+        }
+        ResidualCtx c;
+        c.n_t = Nt;
+        c.n_d = Nd;
+        c.inv_t = dd_recip(Zt);
+        c.inv_d = dd_recip(Zd);
+        c.direct = false;  // (no shared-memory table here: the general weights)
+        c.a_t = c.a_d = dd{0.0f, 0.0f};
+        const ResidualParts rp{tot_t, sub_t, ws_ptr<float4>(p.ws, p.L.rtot) + (size_t)s * cpr, cpr,
+                               Nt, Nd, c.inv_t, c.inv_d};
+        ResidualBlock<DT> fn{trp, drp, p.R.V, c, P};
+        tok = draw_inverse_cdf_parts<ResidualBlock<DT>::PL>(rp, cpr, Geo<DT>::kChunk, Geo<DT>::kSub,
+                                                            u, lane, fn, nullptr);
+        if (tok < 0) {  // the residual has no mass (only through rounding): a draw from p
+            PreciseBlock<DT> fn{trp, p.R.V, P};
+            tok = draw_inverse_cdf_parts<PreciseBlock<DT>::PL>(TargetParts{tot_t, sub_t}, cpr,
+                                                               Geo<DT>::kChunk, Geo<DT>::kSub, u,
+                                                               lane, fn, nullptr);
+        }
+    }
+    if (lane == 0) {
+        if (tok < 0) raise_error(p.ws, kErrNonfinite);
+        p.out_token[s] = tok < 0 ? 0 : tok;
+    }
+}
+
 template <typename Kern>
 static int grid_for(Kern kern, long long warps_needed, size_t smem) {
     int occ = 0;
@@ -266,11 +372,12 @@ static int grid_for(Kern kern, long long warps_needed, size_t smem) {
     return (int)(g < 1 ? 1 : g);
 }
 
-// One warp per sequence (8 per block), launched as a programmatic dependent of the stream before.
-static cudaError_t launch_warp_per_seq(const void* kern, const SampleParams& p, cudaStream_t st) {
+// One warp per sequence, one sequence per block (the draws are long dependent chains: each gets
+// an SM's issue slots to itself), launched as a programmatic dependent of the stream before.
+static cudaError_t launch_warp_per_block(const void* kern, const SampleParams& p, cudaStream_t st) {
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)((p.R.S + 7) / 8));
-    cfg.blockDim = dim3(256);
+    cfg.gridDim = dim3((unsigned)p.R.S);
+    cfg.blockDim = dim3(kWarp);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -291,8 +398,8 @@ static cudaError_t launch_sd_sample_t(const SampleParams& p, cudaStream_t st) {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (p.vec) {
-        // aligned rows: the rows pass and the residual pass as the pipelined stream, each
-        // followed by its per-sequence epilogue as a programmatic dependent
+        // aligned rows: one final-token pass over the (target, draft) row pairs as the pipelined
+        // stream, then the per-sequence draws as a programmatic dependent
         StreamParams sp{};
         sp.R = p.R;
         sp.dtype = DT;
@@ -306,13 +413,9 @@ static cudaError_t launch_sd_sample_t(const SampleParams& p, cudaStream_t st) {
         sp.cpr = p.cpr;
         sp.slots = 2 * p.R.K + 1;
         sp.div_cpr = make_fastdiv((uint32_t)p.cpr);
-        sp.mode = kModeSDRows;
+        sp.mode = kModeSDFinal;
         e = launch_stream_tma(sp, st);
-        if (e == cudaSuccess) e = launch_warp_per_seq(reinterpret_cast<const void*>(sd_rows_finish_kernel<DT>), p, st);
-        if (e != cudaSuccess) return e;
-        sp.mode = kModeSDResidual;
-        e = launch_stream_tma(sp, st);
-        if (e == cudaSuccess) e = launch_warp_per_seq(reinterpret_cast<const void*>(sd_residual_finish_kernel<DT>), p, st);
+        if (e == cudaSuccess) e = launch_warp_per_block(reinterpret_cast<const void*>(sd_final_finish_kernel<DT>), p, st);
         return e;
     }
     k2<<<grid_for(k2, (long long)p.R.S * 2 * p.cpr, smem), kSampleThreads, smem, st>>>(p);

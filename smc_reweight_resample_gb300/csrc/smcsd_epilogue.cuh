@@ -148,7 +148,8 @@ __device__ __forceinline__ bool log_ratio(const StreamParams& p, int k, const fl
 // the row (pair) to draw the final token from. Position k is accepted iff u_k < exp(min(0, l_k)),
 // with the exponential in double-float.
 static __device__ __noinline__ void sd_seq_epilogue(const StreamParams& p, int s, int ks, int lane,
-                                                    const float2* sL, const int* sX, const float* sZ) {
+                                                    const float2* sL, const int* sX, const float* sZ,
+                                                    const Exp2Table& T) {
     const Rows& R = p.R;
     const float* u = p.uniforms + (size_t)s * (R.K + 1);
     int acc = ks;
@@ -162,7 +163,7 @@ static __device__ __noinline__ void sd_seq_epilogue(const StreamParams& p, int s
             if (!ok || !(ell.hi == ell.hi)) {
                 rej = true;
             } else if (ell.hi < 0.0f) {
-                const ddx e = exp_split(ell, p.T);
+                const ddx e = exp_split(ell, T);
                 const float sc = pow2i(e.n);
                 rej = !dd_gt(dd{f_mul(e.hi, sc), f_mul(e.lo, sc)}, dd{uk, 0.0f});
             }  // l_k >= 0: the ratio is at least 1 > u
@@ -177,6 +178,12 @@ static __device__ __noinline__ void sd_seq_epilogue(const StreamParams& p, int s
         st->acc = acc;
         st->trow = trow_of(R, s, acc);
         st->drow = acc < ks ? drow_of(R, s, acc) : -1;
+        // p_i > q_i iff c z_t,i - L_t > c z_d,i - L_d iff z_t,i - z_d,i > (L_t - L_d) / c
+        if (acc < ks) {
+            const float2 Lt = sL[2 * acc], Ld = sL[2 * acc + 1];
+            const dd dl = dd_sub(dd{Lt.x, Lt.y}, dd{Ld.x, Ld.y});
+            st->theta = f_div(f_add(dl.hi, dl.lo), p.sc_t.c_hi);
+        }
     }
 }
 
@@ -333,39 +340,12 @@ __device__ __forceinline__ ResidualCtx residual_ctx(const SeqState* st, const Pr
     return c;
 }
 
-// Chunk of the SD final-token pass (kModeSDRows): precise item i (high bit set) is chunk i % cpr
-// of row `which` = (i / cpr) % 2 of sequence i / (2 cpr) (p.div_seq divides by 2 cpr here): the
-// sequence's target row to draw from (which 0) or its draft row (which 1, needed only for a
-// residual draw). With `rows` the row is looked up in the hand-off state, and a draft row that is
-// not needed (or a sequence that is not valid) makes the item invalid; without, only the indices
-// are decoded. `slot` carries `which`.
-__device__ __forceinline__ ChunkRef chunk_ref_sd_rows(const StreamParams& p, uint32_t tag_item, bool rows) {
-    ChunkRef c;
-    const uint32_t i = tag_item & 0x7fffffffu;
-    c.s = (int)fast_div(i, p.div_seq);
-    const uint32_t rem = i - (uint32_t)c.s * p.div_seq.d;
-    const int which = rem >= (uint32_t)p.cpr ? 1 : 0;
-    c.chunk = (int)rem - which * p.cpr;
-    c.slot = which;
-    c.ks = 0;
-    c.is_draft = which == 1;
-    c.valid = true;
-    c.row = 0;
-    if (rows) {
-        const int ks = seq_len(p.R, c.s, p.ws);
-        const SeqState* st = ws_ptr<SeqState>(p.ws, p.L.seq) + c.s;
-        const int mode = ks >= 0 ? __ldcg(&st->mode) : 0;
-        c.valid = ks >= 0 && !(which == 1 && mode == 0);
-        c.row = c.valid ? (which ? __ldcg(&st->drow) : __ldcg(&st->trow)) : 0;
-    }
-    return c;
-}
-
-// Half item of the SD residual pass (kModeSDResidual): item i (high bit set) is the target
-// (i even) or draft (i odd) chunk of pair i >> 1 = sequence s's chunk `chunk` (pair = s * cpr +
-// chunk). With `rows` the row is looked up in the hand-off state, and a sequence that does not
-// draw a correction token (or is not valid) makes the item invalid. `slot` carries which row.
-__device__ __forceinline__ ChunkRef chunk_ref_sd_residual(const StreamParams& p, uint32_t tag_item, bool rows) {
+// Half item of the SD final-token pass (kModeSDFinal): item i (high bit set) is the target (i
+// even) or draft (i odd) chunk of pair i >> 1 = sequence s's chunk `chunk` (pair = s * cpr +
+// chunk); with `rows` the row is looked up in the hand-off state. Valid for the target half of every
+// sequence and for the draft half of a sequence that draws a correction token; the target row is
+// the one the sequence draws from (its bonus row, or the row of the rejected position).
+__device__ __forceinline__ ChunkRef chunk_ref_sd_final(const StreamParams& p, uint32_t tag_item, bool rows) {
     ChunkRef c;
     const uint32_t i = tag_item & 0x7fffffffu;
     const int which = (int)(i & 1u);
@@ -380,7 +360,7 @@ __device__ __forceinline__ ChunkRef chunk_ref_sd_residual(const StreamParams& p,
     if (rows) {
         const int ks = seq_len(p.R, c.s, p.ws);
         const SeqState* st = ws_ptr<SeqState>(p.ws, p.L.seq) + c.s;
-        c.valid = ks >= 0 && __ldcg(&st->mode) == 1;
+        c.valid = ks >= 0 && (which == 0 || __ldcg(&st->mode) == 1);
         c.row = c.valid ? (which ? __ldcg(&st->drow) : __ldcg(&st->trow)) : 0;
     }
     return c;

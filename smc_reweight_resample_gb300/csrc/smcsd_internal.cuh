@@ -80,7 +80,8 @@ struct SeqState {  // per-sequence hand-off between the SD kernels
     float inv_t_hi, inv_t_lo;  // 1 / (target row total) in units of 2^N_t
     float inv_d_hi, inv_d_lo;
     int n_t, n_d;
-    int pad[2];
+    float theta;  // residual draw: p_i > q_i exactly when z_t,i - z_d,i > theta (to float accuracy)
+    int pad;
 };
 
 struct WsLayout {

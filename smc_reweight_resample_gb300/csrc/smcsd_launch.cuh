@@ -7,11 +7,11 @@
 
 namespace smcsd {
 
-// kModeSDRows: the SD final-token pass over the row (pair) each sequence draws from, all chunks
-// precise, rows looked up in the hand-off state the SD epilogue wrote. kModeSDResidual: the
-// residual pass over the (target, draft) row pairs of the sequences that draw a correction
-// token, a chunk of each row per item.
-enum StreamMode { kModeSD = 0, kModeSMC = 1, kModeSMCStep = 2, kModeSDRows = 3, kModeSDResidual = 4 };
+// kModeSDFinal: the SD final-token pass over (target, draft) chunk pairs: a sequence that drew
+// all its drafts gets the precise partials of its bonus row, one that rejected one gets, per lane
+// block of the pair, the sums of exp(c z_t) and exp(c z_d) over all positions and over the
+// positions where z_t - z_d exceeds theta.
+enum StreamMode { kModeSD = 0, kModeSMC = 1, kModeSMCStep = 2, kModeSDFinal = 5 };
 
 // One streaming pass over all logits rows (SD first pass, SMC reweight, fused SMC step).
 struct StreamParams {

@@ -706,18 +706,27 @@ __device__ __forceinline__ dd part_value(float4 p, int N) {
     return dd{f_mul(p.x, s), f_mul(p.y, s)};
 }
 
-// Draw token = min{ i : sum_{j<=i} w_j > u * sum_j w_j } over a row whose chunk totals `tot`
-// [cpr] and lane-block partials `sub` [cpr * kSubs] describe the weights, rescanning one lane
-// block with `block_weights(chunk, sub, lane, N, w[PL])` (PL = kSub / 32 weights per lane, in
-// units of 2^N, reproducing the partials exactly). Returns the token on every lane (-1 if the
-// row has no mass). If `lse` is given it receives log(sum_j w_j) + N ln 2 (in float). Lane l reads the
-// contiguous chunk totals [l*cpl, l*cpl + cpl) once (kept in registers up to kDrawCache per
-// lane) and serves both the common exponent and the chunk-level walk from them.
+// Records of a row's partials in memory: chunk totals tot [cpr] and lane-block partials
+// sub [cpr * kSubs], each {x, y, n bits, -} = (x + y) 2^n (see pack_part).
+struct ArrayParts {
+    const float4* tot;
+    const float4* sub;
+    __device__ __forceinline__ float4 chunk(int c) const { return ld_cg4(tot + c); }
+    __device__ __forceinline__ float4 block(int c, int l) const { return ld_cg4(sub + (size_t)c * kSubs + l); }
+};
+
+// Draw token = min{ i : sum_{j<=i} w_j > u * sum_j w_j } over a row whose chunk totals
+// (parts.chunk(c), c < cpr) and lane-block partials (parts.block(c, l)) describe the weights,
+// rescanning one lane block with `block_weights(chunk, sub, lane, N, w[PL])` (PL = kSub / 32
+// weights per lane, in units of 2^N, reproducing the partials exactly). Returns the token on
+// every lane (-1 if the row has no mass). If `lse` is given it receives log(sum_j w_j) + N ln 2
+// (in float). Lane l reads the contiguous chunk totals [l*cpl, l*cpl + cpl) once (kept in
+// registers up to kDrawCache per lane) and serves both the common exponent and the chunk-level
+// walk from them.
 constexpr int kDrawCache = 4;
-template <int PL, typename BlockFn>
-__device__ int draw_inverse_cdf(const float4* tot, const float4* sub, int cpr, int chunk_elems,
-                                int sub_elems, float u, int lane, BlockFn block_weights,
-                                float* lse) {
+template <int PL, typename Parts, typename BlockFn>
+__device__ int draw_inverse_cdf_parts(const Parts& parts, int cpr, int chunk_elems, int sub_elems,
+                                      float u, int lane, BlockFn block_weights, float* lse) {
     const int cpl = (cpr + kWarp - 1) / kWarp;
     const int c_begin = min(lane * cpl, cpr), c_end = min(c_begin + cpl, cpr);
     const bool cached = cpl <= kDrawCache;
@@ -726,12 +735,12 @@ __device__ int draw_inverse_cdf(const float4* tot, const float4* sub, int cpr, i
     if (cached) {
 #pragma unroll
         for (int q = 0; q < kDrawCache; ++q) {
-            tc[q] = c_begin + q < c_end ? ld_cg4(tot + c_begin + q) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            tc[q] = c_begin + q < c_end ? parts.chunk(c_begin + q) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
             if (tc[q].x > 0.0f) N = max(N, __float_as_int(tc[q].z));
         }
     } else {
         for (int c = lane; c < cpr; c += kWarp) {
-            const float4 t = ld_cg4(tot + c);
+            const float4 t = parts.chunk(c);
             if (t.x > 0.0f) N = max(N, __float_as_int(t.z));
         }
     }
@@ -745,11 +754,12 @@ __device__ int draw_inverse_cdf(const float4* tot, const float4* sub, int cpr, i
         for (int q = 0; q < kDrawCache; ++q)
             if (c_begin + q < c_end) loc = dd_add(loc, part_value(tc[q], N));
     } else {
-        for (int c = c_begin; c < c_end; ++c) loc = dd_add(loc, part_value(ld_cg4(tot + c), N));
+        for (int c = c_begin; c < c_end; ++c) loc = dd_add(loc, part_value(parts.chunk(c), N));
     }
     const dd excl = warp_exclusive_scan_dd(loc, lane);
     const dd incl = dd_add(excl, loc);
     const dd R{__shfl_sync(0xffffffffu, incl.hi, 31), __shfl_sync(0xffffffffu, incl.lo, 31)};
+    if (!(R.hi > 0.0f)) return -1;  // no mass (a residual whose records are all zero)
     if (lse) *lse = f_add(f_mul((float)N, SMCSD_LN2_HI), f_add(logf(R.hi), f_div(R.lo, R.hi)));
     const dd target = dd_mul_f(R, u);
 
@@ -787,7 +797,7 @@ __device__ int draw_inverse_cdf(const float4* tot, const float4* sub, int cpr, i
             for (int q = 0; q < kDrawCache; ++q)
                 if (c_begin + q < c_end) visit(c_begin + q, part_value(tc[q], N));
         } else {
-            for (int c = c_begin; c < c_end; ++c) visit(c, part_value(ld_cg4(tot + c), N));
+            for (int c = c_begin; c < c_end; ++c) visit(c, part_value(parts.chunk(c), N));
         }
         if (c_star < 0) {
             c_star = last_pos;
@@ -800,7 +810,7 @@ __device__ int draw_inverse_cdf(const float4* tot, const float4* sub, int cpr, i
     block_weights.prefetch(c_star, lane);  // the rescan below reads from this chunk
 
     // lane-block level: one block per lane
-    const dd sv = part_value(ld_cg4(sub + (size_t)c_star * kSubs + lane), N);
+    const dd sv = part_value(parts.block(c_star, lane), N);
     const dd sex = warp_exclusive_scan_dd(sv, lane);
     const dd sbase_l = dd_add(base, sex);
     has = sv.hi > 0.0f && dd_gt(dd_add(sbase_l, sv), target);
@@ -843,6 +853,14 @@ __device__ int draw_inverse_cdf(const float4* tot, const float4* sub, int cpr, i
         tok_q = __shfl_sync(0xffffffffu, lastpos, tok_lane);
     }
     return c_star * chunk_elems + s_star * sub_elems + tok_lane * PL + tok_q;
+}
+
+template <int PL, typename BlockFn>
+__device__ __forceinline__ int draw_inverse_cdf(const float4* tot, const float4* sub, int cpr,
+                                                int chunk_elems, int sub_elems, float u, int lane,
+                                                BlockFn block_weights, float* lse) {
+    return draw_inverse_cdf_parts<PL>(ArrayParts{tot, sub}, cpr, chunk_elems, sub_elems, u, lane,
+                                      block_weights, lse);
 }
 
 // Weights exp(c z) / 2^N of one lane block of a row (the rescan of a precise row).

@@ -176,9 +176,9 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 // slot with the block-local sequence number k = 32 * round + slot and the chunk's index. A lane out
 // of chunks tags its slot kTagDone. The lanes poll their slots together (one non-blocking test per
 // lane per pass), so no lane spins alone while the others wait on it.
-// KIND 0: the two lists of the verify and SMC passes; 1: the SD rows pass (kModeSDRows);
-// 2: the SD residual pass (kModeSDResidual), pairs of slots (2j, 2j+1) holding the target and
-// draft chunk of one pair, pairs dealt round-robin over the blocks.
+// KIND 0: the two lists of the verify and SMC passes; 3: the SD final-token pass
+// (kModeSDFinal), pairs of slots (2j, 2j+1) holding the target and draft chunk of one pair,
+// pairs dealt round-robin over the blocks.
 template <int DT, int KIND>
 __device__ __noinline__ void tma_producer(const StreamParams& p, unsigned char* ring,
                                           uint64_t* full, uint64_t* empty,
@@ -198,16 +198,12 @@ __device__ __noinline__ void tma_producer(const StreamParams& p, unsigned char* 
     const uint32_t Bu = gridDim.x, bu = blockIdx.x;
     Deal d = deal_init(KIND == 0 ? p.n_precise : 0, KIND == 0 ? p.n_fast : 0, p.fper, Bu, bu,
                        (uint32_t)slot, kRing);
-    const uint32_t Qb = deal_share(p.n_precise, Bu, bu);  // (KIND 2: pairs; KIND 1: chunks)
+    const uint32_t Qb = deal_share(p.n_precise, Bu, bu);  // (KIND 3: pairs)
     auto local_item = [&]() -> long long {  // tag item of local chunk d.k, or -1
-        if (KIND == 2) {  // residual pairs: local chunk k is half k & 1 of pair k >> 1
+        if (KIND == 3) {  // final-pass pairs: local chunk k is half k & 1 of pair k >> 1
             const uint32_t jp = d.k >> 1;
             if (jp >= Qb) return -1;
             return (long long)((((jp * Bu + bu) << 1) | (d.k & 1u)) | kPreciseBit);
-        }
-        if (KIND == 1) {  // all precise: items b, b+B, ...
-            if (d.k >= Qb) return -1;
-            return (long long)((d.k * Bu + bu) | kPreciseBit);
         }
         return deal_item(d);
     };
@@ -238,9 +234,8 @@ __device__ __noinline__ void tma_producer(const StreamParams& p, unsigned char* 
             done = true;
             continue;
         }
-        const ChunkRef c = KIND == 1   ? chunk_ref_sd_rows(p, (uint32_t)it, true)
-                           : KIND == 2 ? chunk_ref_sd_residual(p, (uint32_t)it, true)
-                                       : chunk_ref_two_list(p, (uint32_t)it);
+        const ChunkRef c = KIND == 3 ? chunk_ref_sd_final(p, (uint32_t)it, true)
+                                     : chunk_ref_two_list(p, (uint32_t)it);
         const long long off = (long long)c.chunk * kChunkBytes;
         const long long left = row_bytes - off;
         const uint32_t bytes = (uint32_t)(left < kChunkBytes ? left : kChunkBytes);
@@ -267,16 +262,162 @@ __device__ __noinline__ void tma_producer(const StreamParams& p, unsigned char* 
     if (round > 0) mbar_wait(fb, (round - 1) & 1u);
 }
 
-// A consumer warp of the SD residual pass: it claims both slots of a pair (target chunk in the
-// even slot, draft chunk in the odd one), reads the sequence's residual context while the data
-// lands, and stores the double-float sums of max(0, p - q) per lane block and per chunk (residual
-// partials of the residual draw). Lane l reads its block's pieces with an XOR swizzle (piece
-// i ^ (l & 7)), conflict-free.
+// The largest logit of a chunk in a slot (lane l reads its own block), on every lane, and whether
+// a NaN is among them.
 template <int DT>
-__device__ __forceinline__ void residual_consumer(const StreamParams& p, const PreciseCtx& P,
-                                                  unsigned char* ring, uint64_t* full,
-                                                  uint64_t* empty, unsigned long long* tag,
-                                                  unsigned* next, unsigned* n_done, int lane) {
+__device__ __forceinline__ float slot_max(const SharedSrc<DT>& src, bool& nan) {
+    float m = kNegInf;
+    nan = false;
+#pragma unroll
+    for (int i = 0; i < kLoads; ++i) {
+        const uint4 v = src.piece(i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (DT == 1) {
+                const float a = bf16_lo(w[j]), b = bf16_hi(w[j]);
+                m = fmaxf(m, fmaxf(a, b));
+                nan |= (a != a) | (b != b);
+            } else {
+                const float a = __uint_as_float(w[j]);
+                m = fmaxf(m, a);
+                nan |= (a != a);
+            }
+        }
+    }
+    nan = __any_sync(0xffffffffu, nan);
+    return warp_max(m);
+}
+
+// Reference exponent of a chunk whose largest logit is m (kNoMass for a chunk without mass);
+// raises SMCSD_ERR_NONFINITE for NaN, +inf or a scaled logit above the supported range.
+__device__ __forceinline__ int chunk_nref(float m, bool nan, const PreciseCtx& P, int lane) {
+    const float cm = m * P.sc.c_hi;
+    const bool ok = !nan && m > kNegInf && cm >= -kMaxScaledLogit && cm <= kMaxScaledLogit;
+    if (ok) return floor_int(f_mul(m, P.sc.c2));
+    const bool too_big = m > kNegInf && !(cm <= kMaxScaledLogit);
+    if ((nan || too_big) && lane == 0) raise_error(P.ws, kErrNonfinite);
+    return kNoMass;
+}
+
+// The four sums of one lane block of a (target, draft) chunk pair (see final_consumer), in units
+// of 2^nt and 2^nd. With a direct bf16 table (exp(c z) itself in shared memory) and both
+// exponents in its range, a table pass adds the entries of both rows on accumulators biased by
+// 2^(n+2) (as table_pass does), the two halves of every word on separate accumulators, and a
+// second pass adds, through the general weights, the positions outside the table's domain
+// (pieces flagged by the first). Otherwise every position goes through precise_weight.
+template <int DT>
+__device__ __forceinline__ void pair_sums(const SharedSrc<DT>& src_t, const SharedSrc<DT>& src_d,
+                                          int nt, int nd, float theta, const PreciseCtx& P,
+                                          dd& st, dd& sd, dd& sa, dd& sb) {
+    constexpr int PERP = 16 / Geo<DT>::kBytes;
+    st = sd = sa = sb = dd{0.0f, 0.0f};
+    if (!src_t.live()) return;
+    unsigned rare = (1u << kLoads) - 1;  // pieces left to the per-position pass
+    bool covered = false;                // whether the table pass took the in-domain positions
+    if (DT == 1 && P.tab && P.direct && nt != kNoMass && nd != kNoMass && nt >= kDirectMinRef &&
+        nt <= kDirectMaxRef && nd >= kDirectMinRef && nd <= kDirectMaxRef) {
+        covered = true;
+        const uint32_t tab = shared_addr(P.tab);
+        const float bt = pow2i(nt + 2), bd = pow2i(nd + 2);
+        dd t0{bt, 0.0f}, t1{bt, 0.0f}, a0{bt, 0.0f}, a1{bt, 0.0f};
+        dd d0{bd, 0.0f}, d1{bd, 0.0f}, b0{bd, 0.0f}, b1{bd, 0.0f};
+        unsigned pieces = 0;
+#pragma unroll 1
+        for (int i = 0; i < kLoads; ++i) {
+            const uint4 vt = src_t.piece(i), vd = src_d.piece(i);
+            const uint32_t wt[4] = {vt.x, vt.y, vt.z, vt.w}, wd[4] = {vd.x, vd.y, vd.z, vd.w};
+            uint32_t omax = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t ot, od;
+                const uint32_t it = tab_index2(wt[j], ot), id = tab_index2(wd[j], od);
+                asm("max.u16x2 %0, %1, %2;" : "=r"(omax) : "r"(omax), "r"(ot));
+                asm("max.u16x2 %0, %1, %2;" : "=r"(omax) : "r"(omax), "r"(od));
+                const float2 et0 = lds_f2(tab + (it & 0xffffu) * 8u), et1 = lds_f2(tab + (it >> 16) * 8u);
+                const float2 ed0 = lds_f2(tab + (id & 0xffffu) * 8u), ed1 = lds_f2(tab + (id >> 16) * 8u);
+                acc_biased(t0, dd{et0.x, et0.y});
+                acc_biased(t1, dd{et1.x, et1.y});
+                acc_biased(d0, dd{ed0.x, ed0.y});
+                acc_biased(d1, dd{ed1.x, ed1.y});
+                // p_i > q_i (a NaN difference, both masked, is not)
+                const bool c0 = f_sub(bf16_lo(wt[j]), bf16_lo(wd[j])) > theta;
+                const bool c1 = f_sub(bf16_hi(wt[j]), bf16_hi(wd[j])) > theta;
+                acc_biased(a0, c0 ? dd{et0.x, et0.y} : dd{0.0f, 0.0f});
+                acc_biased(b0, c0 ? dd{ed0.x, ed0.y} : dd{0.0f, 0.0f});
+                acc_biased(a1, c1 ? dd{et1.x, et1.y} : dd{0.0f, 0.0f});
+                acc_biased(b1, c1 ? dd{ed1.x, ed1.y} : dd{0.0f, 0.0f});
+            }
+            if ((omax & 0xffffu) >= kTabHalf || (omax >> 16) >= kTabHalf) pieces |= 1u << i;
+            t0 = fast_two_sum(t0.hi, t0.lo);
+            t1 = fast_two_sum(t1.hi, t1.lo);
+            d0 = fast_two_sum(d0.hi, d0.lo);
+            d1 = fast_two_sum(d1.hi, d1.lo);
+            a0 = fast_two_sum(a0.hi, a0.lo);
+            a1 = fast_two_sum(a1.hi, a1.lo);
+            b0 = fast_two_sum(b0.hi, b0.lo);
+            b1 = fast_two_sum(b1.hi, b1.lo);
+        }
+        rare = pieces;
+        const float ft = pow2i(-nt), fd = pow2i(-nd);
+        auto fin = [](dd x, dd y, float bias, float f) {
+            const dd v = dd_add(fast_two_sum(f_sub(x.hi, bias), x.lo), fast_two_sum(f_sub(y.hi, bias), y.lo));
+            return dd{f_mul(v.hi, f), f_mul(v.lo, f)};
+        };
+        st = fin(t0, t1, bt, ft);
+        sd = fin(d0, d1, bd, fd);
+        sa = fin(a0, a1, bt, ft);
+        sb = fin(b0, b1, bd, fd);
+    }
+    if (!rare) return;
+    // positions the table pass did not take (all of them without it), through the general weights
+    dd xt{kBias, 0.0f}, xd{kBias, 0.0f}, xa{kBias, 0.0f}, xb{kBias, 0.0f};
+    do {
+        const int i = __ffs(rare) - 1;
+        rare &= rare - 1;
+        const uint4 vt = src_t.piece(i), vd = src_d.piece(i);
+        const uint32_t wt[4] = {vt.x, vt.y, vt.z, vt.w}, wd[4] = {vd.x, vd.y, vd.z, vd.w};
+#pragma unroll 1
+        for (int q = 0; q < PERP; ++q) {
+            const uint32_t ut = DT == 1 ? ((q & 1) ? (wt[q >> 1] >> 16) : (wt[q >> 1] & 0xffffu)) : wt[q];
+            const uint32_t ud = DT == 1 ? ((q & 1) ? (wd[q >> 1] >> 16) : (wd[q >> 1] & 0xffffu)) : wd[q];
+            const bool in_t = covered && ((ut & 0x7fffu) - kTabMagLo) < kTabHalf;
+            const bool in_d = covered && ((ud & 0x7fffu) - kTabMagLo) < kTabHalf;
+            const dd et = (in_t || nt == kNoMass) ? dd{0.0f, 0.0f} : precise_weight<DT>(ut, nt, P);
+            const dd ed = (in_d || nd == kNoMass) ? dd{0.0f, 0.0f} : precise_weight<DT>(ud, nd, P);
+            acc_biased(xt, et);
+            acc_biased(xd, ed);
+            if (f_sub(bits_to_float<DT>(ut), bits_to_float<DT>(ud)) > theta) {
+                acc_biased(xa, et);
+                acc_biased(xb, ed);
+            }
+        }
+        xt = fast_two_sum(xt.hi, xt.lo);
+        xd = fast_two_sum(xd.hi, xd.lo);
+        xa = fast_two_sum(xa.hi, xa.lo);
+        xb = fast_two_sum(xb.hi, xb.lo);
+    } while (rare);
+    st = dd_add(st, unbias(xt));
+    sd = dd_add(sd, unbias(xd));
+    sa = dd_add(sa, unbias(xa));
+    sb = dd_add(sb, unbias(xb));
+}
+
+// A consumer warp of the SD final-token pass: it claims both slots of a pair (target chunk in the
+// even slot, draft chunk in the odd one). A sequence that accepted every draft has only the
+// target half (its bonus row), whose precise partials go to ddtot/ddsub as in the SMC passes. For
+// a sequence that rejected one, each lane sums over its block of the pair, in double-float
+// units of 2^n_t and 2^n_d (each row's chunk exponent), S_t = sum exp(c z_t), S_d = sum exp(c z_d),
+// A = the same over the positions with z_t - z_d > theta for the target row and B for the draft
+// row: the row normalisers (S_t, S_d) and the residual's mass (A / Z_t - B / Z_d) then come from
+// one read of the pair. Records: ddsub rows 2s and 2s+1 hold {S_t, A} and {S_d, B} per lane block,
+// ddtot rows 2s and 2s+1 the chunk totals of S_t and S_d with their exponents, rtot {A, B} per
+// chunk.
+template <int DT>
+__device__ __forceinline__ void final_consumer(const StreamParams& p, const PreciseCtx& P,
+                                               unsigned char* ring, uint64_t* full, uint64_t* empty,
+                                               unsigned long long* tag, unsigned* next,
+                                               unsigned* n_done, int lane) {
     constexpr int SUB = Geo<DT>::kSub, PERP = 16 / Geo<DT>::kBytes;
     const SeqState* seq = ws_ptr<SeqState>(p.ws, p.L.seq);
     for (;;) {
@@ -296,17 +437,22 @@ __device__ __forceinline__ void residual_consumer(const StreamParams& p, const P
             if (__shfl_sync(0xffffffffu, nd, 0) == (unsigned)kRing) break;
             continue;
         }
-        // both halves of a pair come from the same round of two lanes of one producer warp
         if (!__all_sync(0xffffffffu, tag_wait(smem_u32(&tag[slot1]), k + 1, seen1))) {
             if (lane == 0) raise_error(p.ws, kErrTimeout);
             break;
         }
-        const uint32_t item = (uint32_t)seen0;  // 0xffffffff: nothing loaded
+        seen1 = __shfl_sync(0xffffffffu, seen1, 0);
+        const uint32_t item0 = (uint32_t)seen0, item1 = (uint32_t)seen1;  // 0xffffffff: not loaded
         ChunkRef c{};
         c.valid = false;
-        if (item != 0xffffffffu) c = chunk_ref_sd_residual(p, item, false);
-        ResidualCtx rc{};
-        if (c.valid) rc = residual_ctx(seq + c.s, P);
+        if (item0 != 0xffffffffu) c = chunk_ref_sd_final(p, item0, false);
+        int mode = 0;
+        float theta = 0.0f;
+        if (c.valid) {
+            mode = __ldcg(&seq[c.s].mode);
+            theta = __ldcg(&seq[c.s].theta);
+        }
+        const bool pair = c.valid && mode == 1 && item1 != 0xffffffffu;
         if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full[slot0]), (k / kRing) & 1u) &&
                                          mbar_wait(smem_u32(&full[slot1]), (k / kRing) & 1u))) {
             if (lane == 0) raise_error(p.ws, kErrTimeout);
@@ -317,44 +463,46 @@ __device__ __forceinline__ void residual_consumer(const StreamParams& p, const P
             const long long e0 = (long long)c.chunk * Geo<DT>::kChunk + (long long)lane * SUB;
             unsigned char* bt = ring + (size_t)slot0 * kChunkBytes + lane * 128;
             unsigned char* bd = ring + (size_t)slot1 * kChunkBytes + lane * 128;
-            dd acc{kBias, 0.0f};
-            if (e0 < p.R.V) {
-                if (e0 + SUB > p.R.V) {
-                    // the rows end inside this block: the lane overwrites its logits past V with
-                    // -inf (the rest of the slots holds older chunks)
-                    for (int q = 0; q < SUB; ++q)
-                        if (e0 + q >= p.R.V) {
-                            if (DT == 1) {
-                                reinterpret_cast<unsigned short*>(bt)[q] = 0xff80u;
-                                reinterpret_cast<unsigned short*>(bd)[q] = 0xff80u;
-                            } else {
-                                reinterpret_cast<uint32_t*>(bt)[q] = 0xff800000u;
-                                reinterpret_cast<uint32_t*>(bd)[q] = 0xff800000u;
-                            }
+            if (c.chunk == p.cpr - 1 && e0 + SUB > p.R.V) {
+                // the rows end inside this block: the lane overwrites its logits past V with -inf
+                // (the rest of the slots holds older chunks)
+                for (int q = 0; q < SUB; ++q)
+                    if (e0 + q >= p.R.V) {
+                        if (DT == 1) {
+                            reinterpret_cast<unsigned short*>(bt)[q] = 0xff80u;
+                            reinterpret_cast<unsigned short*>(bd)[q] = 0xff80u;
+                        } else {
+                            reinterpret_cast<uint32_t*>(bt)[q] = 0xff800000u;
+                            reinterpret_cast<uint32_t*>(bd)[q] = 0xff800000u;
                         }
-                    wrote = true;
-                }
-                const int sw = lane & 7;
-#pragma unroll 1
-                for (int i = 0; i < kLoads; ++i) {
-                    const uint4 vt = *reinterpret_cast<const uint4*>(bt + ((i ^ sw) << 4));
-                    const uint4 vd = *reinterpret_cast<const uint4*>(bd + ((i ^ sw) << 4));
-                    const uint32_t wt[4] = {vt.x, vt.y, vt.z, vt.w}, wd[4] = {vd.x, vd.y, vd.z, vd.w};
-#pragma unroll
-                    for (int q = 0; q < PERP; ++q) {
-                        const uint32_t xt = DT == 1 ? ((q & 1) ? (wt[q >> 1] >> 16) : (wt[q >> 1] & 0xffffu)) : wt[q];
-                        const uint32_t xd = DT == 1 ? ((q & 1) ? (wd[q >> 1] >> 16) : (wd[q >> 1] & 0xffffu)) : wd[q];
-                        acc_biased(acc, residual_weight<DT>(xt, xd, rc, P));
                     }
-                    acc = fast_two_sum(acc.hi, acc.lo);
+                wrote = true;
+            }
+            const size_t prow = (size_t)c.s * 2;
+            float4* tot_t = ws_ptr<float4>(p.ws, p.L.ddtot) + prow * p.cpr + c.chunk;
+            float4* sub_t = ws_ptr<float4>(p.ws, p.L.ddsub) + (prow * p.cpr + c.chunk) * kSubs;
+            const SharedSrc<DT> src_t{bt, lane & 7, e0 < p.R.V};
+            if (!pair) {
+                precise_core<DT>(src_t, src_t, lane, P, tot_t, sub_t);
+            } else {
+                const SharedSrc<DT> src_d{bd, lane & 7, e0 < p.R.V};
+                bool nan_t, nan_d;
+                const float mt = slot_max<DT>(src_t, nan_t), md = slot_max<DT>(src_d, nan_d);
+                const int nt = chunk_nref(mt, nan_t, P, lane), nd = chunk_nref(md, nan_d, P, lane);
+                dd vst, vsd, va, vb;
+                pair_sums<DT>(src_t, src_d, nt, nd, theta, P, vst, vsd, va, vb);
+                float4* sub_d = sub_t + (size_t)p.cpr * kSubs;
+                sub_t[lane] = make_float4(vst.hi, vst.lo, va.hi, va.lo);
+                sub_d[lane] = make_float4(vsd.hi, vsd.lo, vb.hi, vb.lo);
+                const dd tst = warp_sum_dd(vst), tsd = warp_sum_dd(vsd);
+                const dd ta = warp_sum_dd(va), tb = warp_sum_dd(vb);
+                if (lane == 0) {
+                    *tot_t = pack_part(tst, nt);
+                    tot_t[p.cpr] = pack_part(tsd, nd);
+                    ws_ptr<float4>(p.ws, p.L.rtot)[(size_t)c.s * p.cpr + c.chunk] =
+                        make_float4(ta.hi, ta.lo, tb.hi, tb.lo);
                 }
             }
-            const dd sv = unbias(acc);
-            float4* tot = ws_ptr<float4>(p.ws, p.L.rtot) + (size_t)c.s * p.cpr;
-            float4* sub = ws_ptr<float4>(p.ws, p.L.rsub) + (size_t)c.s * p.cpr * kSubs;
-            sub[(size_t)c.chunk * kSubs + lane] = pack_part(sv, 0);
-            const dd total = warp_sum_dd(sv);
-            if (lane == 0) tot[c.chunk] = pack_part(total, 0);
             // stores into a slot must be ordered before the copy engine's next write to it
             if (wrote) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
@@ -376,6 +524,7 @@ template <int DT, int MODE>
 __global__ void __launch_bounds__(kTmaThreads, 1)
     stream_tma_kernel(const __grid_constant__ StreamParams p) {
     constexpr bool kPrecise = MODE != kModeSD;
+    constexpr int kKind = MODE == kModeSDFinal ? 3 : 0;
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* ring = smem;
     float2* sTab = reinterpret_cast<float2*>(smem + kSmemRing);
@@ -406,8 +555,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     if (threadIdx.x == 0) griddep_launch_dependents();
     if (warp < kTmaProducers) {
         constexpr int kPer = kRing / kTmaProducers;
-        tma_producer<DT, MODE == kModeSDRows ? 1 : MODE == kModeSDResidual ? 2 : 0>(
-            p, ring, full, empty, tag, n_done, warp * kPer + (lane % kPer), lane < kPer);
+        tma_producer<DT, kKind>(p, ring, full, empty, tag, n_done, warp * kPer + (lane % kPer),
+                                lane < kPer);
         return;
     }
 
@@ -424,8 +573,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                         ws_ptr<float2>(p.ws, p.L.tab + 16), p.direct, tid, nthr, 1);
         P.tab = sTab;
     }
-    if (MODE == kModeSDResidual) {
-        residual_consumer<DT>(p, P, ring, full, empty, tag, next, n_done, lane);
+    if (MODE == kModeSDFinal) {
+        final_consumer<DT>(p, P, ring, full, empty, tag, next, n_done, lane);
         return;
     }
     for (;;) {
@@ -454,14 +603,14 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         ChunkRef c{};
         c.valid = false;
         if (item != 0xffffffffu)
-            c = MODE == kModeSDRows ? chunk_ref_sd_rows(p, item, false) : chunk_ref_two_list(p, item);
+            c = chunk_ref_two_list(p, item);
         const int s = c.valid ? c.s : -1, rs = c.slot, ks = c.ks, chunk = c.chunk;
         const bool is_draft = c.is_draft;
         const unsigned char* cbuf = ring + (size_t)slot * kChunkBytes;
         const bool sane = s < 0 || (check_ok(p.ws, chunk >= 0 && chunk < p.cpr, -111, chunk) &&
-                                    check_ok(p.ws, rs >= 0 && rs < (MODE == kModeSDRows ? 2 : p.slots), -112, rs));
+                                    check_ok(p.ws, rs >= 0 && rs < p.slots, -112, rs));
         if (s >= 0 && sane) {
-            if (MODE != kModeSDRows && (!kPrecise || rs != 2 * ks)) {
+            if (!kPrecise || rs != 2 * ks) {
                 uint4 raw[kLoads];
 #pragma unroll
                 for (int v = 0; v < kLoads; ++v)
@@ -501,8 +650,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                             else reinterpret_cast<uint32_t*>(blk)[q] = 0xff800000u;
                         }
                 }
-                // sampled rows sit at 2s (SMC: the bonus row; SD: the target row) and 2s + 1
-                const size_t prow = (size_t)(s * 2 + (MODE == kModeSDRows ? rs : 0));
+                // the sampled row of sequence s (its bonus row) has its records at row 2s
+                const size_t prow = (size_t)(s * 2);
                 float4* tot = ws_ptr<float4>(p.ws, p.L.ddtot) + prow * p.cpr + chunk;
                 float4* sub = ws_ptr<float4>(p.ws, p.L.ddsub) + (prow * p.cpr + chunk) * kSubs;
                 const SharedSrc<DT> src{blk, lane & 7, e0 < p.R.V};
@@ -527,19 +676,13 @@ template <int DT, int MODE>
 static cudaError_t launch_tma_t(const StreamParams& p0, cudaStream_t st) {
     auto kern = stream_tma_kernel<DT, MODE>;
     StreamParams p = p0;
-    if (MODE == kModeSDResidual) {
+    if (MODE == kModeSDFinal) {
         // (target, draft) chunk pairs of every sequence; n_precise counts pairs
         p.fslots = 0;
+        p.fper = 0;
         p.n_precise = (long long)p.R.S * p.cpr;
         p.n_fast = 0;
         p.div_fseq = make_fastdiv(1u);
-    } else if (MODE == kModeSDRows) {
-        // two rows per sequence (the second only when its draw needs it), all precise
-        p.fslots = 0;
-        p.n_precise = (long long)p.R.S * 2 * p.cpr;
-        p.n_fast = 0;
-        p.div_fseq = make_fastdiv(1u);
-        p.div_seq = make_fastdiv((uint32_t)(2 * p.cpr));
     } else {
         // the sampled rows (one per particle) form the precise list; in SD mode every row is fast
         const bool sampled = MODE != kModeSD;
@@ -553,7 +696,7 @@ static cudaError_t launch_tma_t(const StreamParams& p0, cudaStream_t st) {
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     const long long cap = device_sm_count();
-    const long long units = (MODE == kModeSDResidual ? 2 : 1) * p.n_precise + p.n_fast;
+    const long long units = (MODE == kModeSDFinal ? 2 : 1) * p.n_precise + p.n_fast;
     const long long want = (units + kTmaConsumers - 1) / kTmaConsumers;
     int grid = (int)(want < cap ? want : cap);
     if (grid < 1) grid = 1;
@@ -579,10 +722,8 @@ cudaError_t launch_wait_selftest(void* ws, unsigned long long limit_ns, cudaStre
 }
 
 cudaError_t launch_stream_tma(const StreamParams& p, cudaStream_t st) {
-    if (p.mode == kModeSDRows)
-        return p.dtype == 0 ? launch_tma_t<0, kModeSDRows>(p, st) : launch_tma_t<1, kModeSDRows>(p, st);
-    if (p.mode == kModeSDResidual)
-        return p.dtype == 0 ? launch_tma_t<0, kModeSDResidual>(p, st) : launch_tma_t<1, kModeSDResidual>(p, st);
+    if (p.mode == kModeSDFinal)
+        return p.dtype == 0 ? launch_tma_t<0, kModeSDFinal>(p, st) : launch_tma_t<1, kModeSDFinal>(p, st);
     if (p.dtype == 0) {
         if (p.mode == kModeSD) return launch_tma_t<0, kModeSD>(p, st);
         if (p.mode == kModeSMC) return launch_tma_t<0, kModeSMC>(p, st);
