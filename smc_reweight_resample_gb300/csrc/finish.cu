@@ -35,9 +35,14 @@ __device__ __forceinline__ void group_part(const StreamParams& p, int g, int32_t
         float* ess = p.ess ? p.ess + g : nullptr;
         int32_t* rs = p.resampled ? p.resampled + g : nullptr;
         const float U = __ldg(p.resample_uniforms + g);
-        int a[1];
-        const bool res = group_resample_small<1>(lw, N, p.ess_threshold, U, anc, ess, rs, p.ws, lane, T, a);
-        if (lane < N) sAnc[lane] = a[0];
+        int a0;
+        bool res;
+        if (!group_resample_fast(lw, N, p.ess_threshold, U, anc, ess, rs, lane, a0, res)) {
+            int a[1];
+            res = group_resample_small<1>(lw, N, p.ess_threshold, U, anc, ess, rs, p.ws, lane, T, a);
+            a0 = a[0];
+        }
+        if (lane < N) sAnc[lane] = a0;
         if (lane == 0) *sRes = res ? 1 : 0;
     }
     bar_sync(bar, nthr);

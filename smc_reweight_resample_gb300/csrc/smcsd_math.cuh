@@ -120,6 +120,18 @@ SMCSD_HD dd dd_recip(dd a) {
     dd c = dd_mul_f(e, r0);
     return dd_add(dd{r0, 0.0f}, c);
 }
+// a / b by long division on the float quotient: q1 = a.hi / b.hi, then two correction digits
+// from the exact remainders a - q1 b and a - (q1 + q2) b. A quotient that is a float (25 / 5) comes
+// out exact, so that a ratio compared with a threshold it equals is not off by the last digit.
+SMCSD_HD dd dd_div(dd a, dd b) {
+    const float q1 = f_div(a.hi, b.hi);
+    dd r = dd_sub(a, dd_mul_f(b, q1));
+    const float q2 = f_div(r.hi, b.hi);
+    r = dd_sub(r, dd_mul_f(b, q2));
+    const float q3 = f_div(r.hi, b.hi);
+    const dd q = fast_two_sum(q1, q2);
+    return dd_add(q, dd{q3, 0.0f});
+}
 // a > b for normalised double-floats.
 SMCSD_HD bool dd_gt(dd a, dd b) { return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo); }
 SMCSD_HD double dd_to_double(dd a) { return (double)a.hi + (double)a.lo; }

@@ -997,7 +997,7 @@ __device__ __forceinline__ bool group_resample_small(float* logw, int N, float t
         }
     }
     const dd W = warp_sum_dd(loc), W2 = warp_sum_dd(loc2);
-    const dd ess = dd_mul(dd_mul(W, W), dd_recip(W2));
+    const dd ess = dd_div(dd_mul(W, W), W2);
     const bool res = dd_gt(dd{thr, 0.0f}, ess);  // ESS < threshold
     if (lane == 0) {
         if (ess_out) *ess_out = f_add(ess.hi, ess.lo);
@@ -1045,6 +1045,70 @@ __device__ __forceinline__ bool group_resample_small(float* logw, int N, float t
 #pragma unroll
     for (int q = 0; q < PER; ++q)
         if (i0 + q < i1) logw[i0 + q] = 0.0f;
+    return true;
+}
+
+// First attempt at the resampling of a group of at most kWarp particles (particle i on lane i), in
+// float arithmetic, for the fused step's group part, whose single-warp chain sits on the step's
+// critical path: w_i = exp(logw_i - max), ESS = W^2 / W2 with W = sum w_i, W2 = sum w_i^2, and
+// ancestors a_j = #{ i : C_i <= v_j }, C_i = (w_0 + ... + w_i) / W, v_j = (j + U) / N, i.e.
+// a_j = #{ i : x_i <= j } with x_i = C_i N - U. The rounding of each quantity is bounded (w_i and
+// W within 1.3e-6 relative, W2 3.3e-6, ESS 6.1e-6, x_i N 2.7e-6 + 1e-6 absolute), and a decision
+// is kept only when it lies farther from its boundary than a margin of about three times that
+// bound: ESS not within 2e-5 relative of the threshold, and no x_i (i < N - 1; C_{N-1} = 1
+// exactly) within 1e-5 (N + 1) of an integer. A kept decision is therefore the exact one, the same
+// as the double-float path's. Otherwise (or for a weight that is not finite) nothing is written
+// and false is returned; the caller then runs group_resample_small. On success writes what
+// group_resample_small writes and returns true, with the lane's ancestor in anc_lane and the
+// resampling flag in res (every lane).
+__device__ __forceinline__ bool group_resample_fast(float* logw, int N, float thr, float U, int32_t* anc,
+                                                    float* ess_out, int32_t* res_out, int lane,
+                                                    int& anc_lane, bool& res) {
+    const bool live = lane < N;
+    const float v = live ? __ldcg(logw + lane) : kNegInf;
+    if (!__all_sync(0xffffffffu, !live || (v == v && v != kPosInf))) return false;
+    const float M = warp_max(v);
+    if (M == kNegInf) return false;
+    const float w = v > kNegInf ? expf(v - M) : 0.0f;
+    const float W = __shfl_sync(0xffffffffu, warp_sum(w), 0);
+    const float W2 = __shfl_sync(0xffffffffu, warp_sum(w * w), 0);
+    const float ess = W * W / W2;
+    if (!(fabsf(ess - thr) > 2e-5f * ess)) return false;  // (also catches a NaN)
+    res = ess < thr;
+    if (!res) {
+        anc_lane = lane;
+        if (live) anc[lane] = lane;
+        if (lane == 0) {
+            if (ess_out) *ess_out = ess;
+            if (res_out) *res_out = 0;
+        }
+        return true;
+    }
+    float S = w;  // inclusive prefix sum
+#pragma unroll
+    for (int o = 1; o < kWarp; o <<= 1) {
+        const float t = __shfl_up_sync(0xffffffffu, S, o);
+        if (lane >= o) S += t;
+    }
+    const float fN = (float)N;
+    const float x = fmaf(S / W, fN, -U);
+    const bool near = live && lane < N - 1 && fabsf(x - rintf(x)) <= 1e-5f * (fN + 1.0f);
+    if (__any_sync(0xffffffffu, near)) return false;
+    // k_i = ceil(x_i): particle i is counted by the children j >= k_i (never for i >= N - 1)
+    const float k = lane < N - 1 ? ceilf(x) : 2.0f * fN;
+    int a = lane;
+    for (int j = 0; j < N; ++j) {
+        const int c = __popc(__ballot_sync(0xffffffffu, k <= (float)j));
+        if (lane == j) a = c < N - 1 ? c : N - 1;
+    }
+    anc_lane = a;
+    if (live) anc[lane] = a;
+    if (lane == 0) {
+        if (ess_out) *ess_out = ess;
+        if (res_out) *res_out = 1;
+    }
+    __syncwarp();
+    if (live) logw[lane] = 0.0f;
     return true;
 }
 
@@ -1133,6 +1197,11 @@ static __device__ __noinline__ bool group_resample_general(float* logw, int N, f
 __device__ __forceinline__ bool group_resample(float* logw, int N, float thr, float U, int32_t* anc,
                                                float* ess_out, int32_t* res_out, void* ws, int lane,
                                                const Exp2Table& T) {
+    if (N <= kWarp) {
+        int a;
+        bool res;
+        if (group_resample_fast(logw, N, thr, U, anc, ess_out, res_out, lane, a, res)) return res;
+    }
     if (N <= kWarp * kResamplePer) {
         int anc_reg[kResamplePer];
         return group_resample_small(logw, N, thr, U, anc, ess_out, res_out, ws, lane, T, anc_reg);

@@ -19,6 +19,15 @@ extern "C" void probe_dd_recip(const float* ah, const float* al, int n, float* r
     }
 }
 
+extern "C" void probe_dd_div(const float* ah, const float* al, const float* bh, const float* bl, int n,
+                             float* qh, float* ql) {
+    for (int i = 0; i < n; ++i) {
+        smcsd::dd q = smcsd::dd_div(smcsd::dd{ah[i], al[i]}, smcsd::dd{bh[i], bl[i]});
+        qh[i] = q.hi;
+        ql[i] = q.lo;
+    }
+}
+
 #include "smcsd_fastdiv.h"
 
 // q = n / d through the launch-invariant division, for n in [0, count).

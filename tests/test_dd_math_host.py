@@ -76,6 +76,33 @@ def test_dd_recip(probe):
     assert err.max() < 1e-13
 
 
+def _dd_div(lib, ah, al, bh, bl):
+    lib.probe_dd_div.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int] + [ctypes.c_void_p] * 2
+    args = [np.ascontiguousarray(x, np.float32) for x in (ah, al, bh, bl)]
+    qh, ql = np.zeros_like(args[0]), np.zeros_like(args[0])
+    lib.probe_dd_div(*[x.ctypes.data for x in args], args[0].size, qh.ctypes.data, ql.ctypes.data)
+    return qh, ql
+
+
+@pytest.mark.skipif(np.finfo(np.longdouble).eps > 1e-18, reason="needs extended long double")
+def test_dd_div(probe):
+    rng = np.random.default_rng(4)
+    ah = rng.uniform(0.5, 3e4, 20000).astype(np.float32)
+    al = (ah * rng.uniform(-2 ** -25, 2 ** -25, ah.size)).astype(np.float32)
+    bh = rng.uniform(0.5, 3e4, ah.size).astype(np.float32)
+    bl = (bh * rng.uniform(-2 ** -25, 2 ** -25, ah.size)).astype(np.float32)
+    qh, ql = _dd_div(probe, ah, al, bh, bl)
+    ld = np.longdouble
+    want = (ah.astype(ld) + al.astype(ld)) / (bh.astype(ld) + bl.astype(ld))
+    assert (np.abs((qh.astype(ld) + ql.astype(ld)) / want - 1)).max() < 1e-13
+    # quotients that are floats come out exact (an ESS of N^2 / N against a threshold of N)
+    n = np.arange(1, 1001, dtype=np.float32)
+    qh, ql = _dd_div(probe, n * n, np.zeros_like(n), n, np.zeros_like(n))
+    assert (qh == n).all() and (ql == 0).all()
+    qh, ql = _dd_div(probe, np.float32([1.0, 3.0, 0.75]), np.zeros(3), np.float32([4.0, 8.0, 3.0]), np.zeros(3))
+    assert qh.tolist() == [0.25, 0.375, 0.25] and (ql == 0).all()
+
+
 @pytest.mark.parametrize("d", [1, 2, 3, 5, 7, 63, 64, 65, 126, 567, 1152, 4097, 72576, 1 << 20, 999983,
                                (1 << 30) + 3])
 def test_fast_division(probe, d):

@@ -108,6 +108,24 @@ def test_ess_resample(smcsd, G, N):
     L.finish()
 
 
+@pytest.mark.parametrize("N", [5, 16, 32])
+def test_ess_resample_on_decision_boundaries(smcsd, N):
+    """Equal log-weights put the ESS exactly on a threshold of N and, with U = 0, every C_i on a
+    point (j + U) / N of the systematic grid: groups of at most one warp then leave their float
+    first attempt for the double-float path, which must still take the exact decisions."""
+    G = 3
+    for thr, U0 in ((float(N), 0.5), (N + 1.0, 0.0), (N + 1.0, 0.5)):
+        lw0 = np.zeros(G * N, np.float32)
+        U = np.full(G, U0, np.float32)
+        lw = dev(lw0.copy())
+        anc, ess, res = smcsd.smc_ess_resample(lw, G, N, thr, dev(U))
+        o = oracle.ess_resample(lw0, G, N, thr, U)
+        np.testing.assert_array_equal(host(res), o["resampled"])
+        np.testing.assert_array_equal(host(anc), o["ancestors"])
+        np.testing.assert_allclose(host(ess), o["ess"], rtol=1e-6, atol=0)
+        np.testing.assert_allclose(host(lw), o["logw"], atol=0, rtol=0)
+
+
 def test_remap(smcsd):
     G, N, P = 8, 16, 128
     rng = np.random.default_rng(4)
