@@ -190,8 +190,8 @@ static __device__ __noinline__ void sd_seq_epilogue(const StreamParams& p, int s
 // SMC: log-weight update sum_k log pi_k(x_k) - log q_k(x_k) of particle s (double-float sums),
 // from its old log-weight lw_old. With the whole-sequence power target the terms are
 // alpha log p_k(x_k) - log q_k(x_k), plus the (K+1)-th token's factor that its row epilogue left
-// in sL[2K]; a log-reward adds reward_scale * log_reward[s].
-static __device__ __noinline__ void smc_particle_epilogue(const StreamParams& p, int s, int lane, float lw_old,
+// in sL[2K]; a log-reward adds reward_scale * log_reward[s]. Returns the new log-weight on lane 0.
+static __device__ __noinline__ float smc_particle_epilogue(const StreamParams& p, int s, int lane, float lw_old,
                                                           const float2* sL, const int* sX, const float* sZ) {
     dd inc{0.0f, 0.0f};
     for (int k = lane; k < p.R.K; k += kWarp) {
@@ -211,8 +211,11 @@ static __device__ __noinline__ void smc_particle_epilogue(const StreamParams& p,
             inc = dd_add(inc, two_prod(p.reward_scale, r));
         }
         const dd lw = dd_add(dd{lw_old, 0.0f}, inc);
-        p.logw[s] = f_add(lw.hi, lw.lo);
+        const float v = f_add(lw.hi, lw.lo);
+        p.logw[s] = v;
+        return v;
     }
+    return 0.0f;
 }
 
 // The fused step's refcount array set to zero by the streaming pass (grid-stride), so that the
@@ -226,17 +229,20 @@ __device__ __forceinline__ void zero_refcount(const StreamParams& p) {
 
 // Page-table rows of one group after resampling, by threads 0..nthr-1 of a block: row j of the output
 // is row anc[j] of the input (row j when the group was not resampled), W ints per access; every
-// non-empty page id is counted in refcount.
+// non-empty page id is counted in refcount. The input rows are read from `tin` (global memory),
+// or from the block's staged copy `stage` (shared memory, the same layout) when it is given.
 template <int W>
 __device__ __forceinline__ void remap_rows_block(const StreamParams& p, const int32_t* tin, int32_t* tout,
-                                                 const int32_t* anc, bool res, int N, int P, int nthr) {
+                                                 const int32_t* anc, bool res, int N, int P, int nthr,
+                                                 const int32_t* stage = nullptr) {
     using Vec = typename std::conditional<W == 4, int4, int>::type;
     const unsigned PW = (unsigned)(P / W);
     const unsigned n = (unsigned)N * PW;
     for (unsigned e = threadIdx.x; e < n; e += (unsigned)nthr) {
         const unsigned j = e / PW, col = e - j * PW;
         const int a = res ? anc[j] : (int)j;
-        const Vec v = __ldg(reinterpret_cast<const Vec*>(tin + (size_t)a * P) + col);
+        const Vec v = stage ? reinterpret_cast<const Vec*>(stage + (size_t)a * P)[col]
+                            : __ldg(reinterpret_cast<const Vec*>(tin + (size_t)a * P) + col);
         reinterpret_cast<Vec*>(tout + (size_t)j * P)[col] = v;
         if (!p.refcount) continue;
         const int32_t* ids = reinterpret_cast<const int32_t*>(&v);

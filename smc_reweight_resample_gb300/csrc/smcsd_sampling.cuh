@@ -954,11 +954,13 @@ __device__ __forceinline__ dd shfl_pick_dd(const dd (&v)[PER], int per, int src,
     return r;
 }
 
+// The log-weights are read from `logw` (global memory), or from lw_in (shared memory) when it is
+// given; the zeros after a resampling always go to `logw`.
 template <int PER>
 __device__ __forceinline__ bool group_resample_small(float* logw, int N, float thr, float U,
                                                      int32_t* anc, float* ess_out, int32_t* res_out,
                                                      void* ws, int lane, const Exp2Table& T,
-                                                     int (&anc_reg)[PER]) {
+                                                     int (&anc_reg)[PER], const float* lw_in = nullptr) {
     const int per = (N + kWarp - 1) / kWarp;
     const int i0 = min(lane * per, N), i1 = min(i0 + per, N);
 #pragma unroll
@@ -970,7 +972,7 @@ __device__ __forceinline__ bool group_resample_small(float* logw, int N, float t
     for (int q = 0; q < PER; ++q) {
         v[q] = kNegInf;
         if (i0 + q < i1) {
-            v[q] = __ldcg(logw + i0 + q);
+            v[q] = lw_in ? lw_in[i0 + q] : __ldcg(logw + i0 + q);
             if (v[q] != v[q] || v[q] == kPosInf) bad = true;
             m = fmaxf(m, v[q]);
         }
@@ -1060,12 +1062,13 @@ __device__ __forceinline__ bool group_resample_small(float* logw, int N, float t
 // as the double-float path's. Otherwise (or for a weight that is not finite) nothing is written
 // and false is returned; the caller then runs group_resample_small. On success writes what
 // group_resample_small writes and returns true, with the lane's ancestor in anc_lane and the
-// resampling flag in res (every lane).
+// resampling flag in res (every lane). The log-weights are read from lw_in (shared memory) when it
+// is given.
 __device__ __forceinline__ bool group_resample_fast(float* logw, int N, float thr, float U, int32_t* anc,
                                                     float* ess_out, int32_t* res_out, int lane,
-                                                    int& anc_lane, bool& res) {
+                                                    int& anc_lane, bool& res, const float* lw_in = nullptr) {
     const bool live = lane < N;
-    const float v = live ? __ldcg(logw + lane) : kNegInf;
+    const float v = live ? (lw_in ? lw_in[lane] : __ldcg(logw + lane)) : kNegInf;
     if (!__all_sync(0xffffffffu, !live || (v == v && v != kPosInf))) return false;
     const float M = warp_max(v);
     if (M == kNegInf) return false;
