@@ -190,12 +190,17 @@ __device__ __forceinline__ dd precise_weight(uint32_t b, int nref, const Precise
 }
 
 // Accumulate y (0 <= y <= ~2) into a biased accumulator whose high part stays >= 4, so that
-// Dekker's fast-two-sum is exact.
+// Dekker's fast-two-sum is exact. One packed f32x2 add forms both acc.hi + y.hi and
+// acc.lo + y.lo; the exact rounding error of the first then joins the low part.
 constexpr float kBias = 4.0f;
 __device__ __forceinline__ void acc_biased(dd& acc, dd y) {
-    const float s = f_add(acc.hi, y.hi);
+    float s, x;
+    asm("{\n .reg .b64 a, b, c;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n"
+        " add.rn.f32x2 c, a, b;\n mov.b64 {%0, %1}, c;\n}"
+        : "=f"(s), "=f"(x)
+        : "f"(acc.hi), "f"(acc.lo), "f"(y.hi), "f"(y.lo));
     const float err = f_sub(y.hi, f_sub(s, acc.hi));
-    acc.lo = f_add(acc.lo, f_add(err, y.lo));
+    acc.lo = f_add(x, err);
     acc.hi = s;
 }
 __device__ __forceinline__ dd unbias(dd acc) { return fast_two_sum(f_sub(acc.hi, kBias), acc.lo); }
@@ -614,7 +619,7 @@ __device__ __forceinline__ void precise_core(const Src& src, const Again& again,
         sv = dd_add(sv, unbias(acc));
     }
     sub_out[lane] = pack_part(sv, nref);
-    const dd total = warp_sum_dd(sv);
+    const dd total = warp_total_fixed(sv);
     if (lane == 0) *tot_out = pack_part(total, nref);
 }
 

@@ -494,8 +494,8 @@ __device__ __forceinline__ void final_consumer(const StreamParams& p, const Prec
                 float4* sub_d = sub_t + (size_t)p.cpr * kSubs;
                 sub_t[lane] = make_float4(vst.hi, vst.lo, va.hi, va.lo);
                 sub_d[lane] = make_float4(vsd.hi, vsd.lo, vb.hi, vb.lo);
-                const dd tst = warp_sum_dd(vst), tsd = warp_sum_dd(vsd);
-                const dd ta = warp_sum_dd(va), tb = warp_sum_dd(vb);
+                const dd tst = warp_total_fixed(vst), tsd = warp_total_fixed(vsd);
+                const dd ta = warp_total_fixed(va), tb = warp_total_fixed(vb);
                 if (lane == 0) {
                     *tot_t = pack_part(tst, nt);
                     tot_t[p.cpr] = pack_part(tsd, nd);
