@@ -41,6 +41,12 @@ constexpr size_t kSmemBytes =
     kSmemRing + kSmemTab + sizeof(Exp2Table) + 2 * kRing * 8 + kRing * 8 + 16;
 constexpr uint32_t kTagNone = 0xffffffffu;  // slot never loaded
 constexpr uint32_t kTagDone = 0xfffffffeu;  // the slot's producer lane has no more chunks
+// The tag word of a fast chunk (no kPreciseBit) carries what its consumer needs, decoded once by
+// the producer (which decodes the chunk's list index anyway to address the copy): the index of
+// the chunk's partial, (s * slots + row slot) * cpr + chunk, below 2^29 (2^29 chunks of 4 KB
+// would be 2 TiB of logits), whether the row is a draft row, and whether the chunk is the row's
+// last.
+constexpr uint32_t kFastTailBit = 1u << 30, kFastDraftBit = 1u << 29, kFastIndexMask = kFastDraftBit - 1u;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -254,7 +260,11 @@ __device__ __noinline__ void tma_producer(const StreamParams& p, unsigned char* 
         } else {
             mbar_arrive_relaxed(fb);
         }
-        tag_store(tb, round * kRing + (uint32_t)slot, (c.valid && sane) ? (uint32_t)it : 0xffffffffu);
+        uint32_t word = (c.valid && sane) ? (uint32_t)it : 0xffffffffu;
+        if (KIND == 0 && c.valid && sane && !(word & kPreciseBit))
+            word = (uint32_t)(((long long)c.s * p.slots + c.slot) * p.cpr + c.chunk) |
+                   (c.is_draft ? kFastDraftBit : 0u) | (c.chunk == p.cpr - 1 ? kFastTailBit : 0u);
+        tag_store(tb, round * kRing + (uint32_t)slot, word);
         ++round;
         deal_advance(d, kRing);
     }
@@ -600,17 +610,14 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             break;
         }
         const uint32_t item = (uint32_t)seen;  // 0xffffffff: a chunk with nothing to load
-        ChunkRef c{};
-        c.valid = false;
-        if (item != 0xffffffffu)
-            c = chunk_ref_two_list(p, item);
-        const int s = c.valid ? c.s : -1, rs = c.slot, ks = c.ks, chunk = c.chunk;
-        const bool is_draft = c.is_draft;
         const unsigned char* cbuf = ring + (size_t)slot * kChunkBytes;
-        const bool sane = s < 0 || (check_ok(p.ws, chunk >= 0 && chunk < p.cpr, -111, chunk) &&
-                                    check_ok(p.ws, rs >= 0 && rs < p.slots, -112, rs));
-        if (s >= 0 && sane) {
-            if (!kPrecise || rs != 2 * ks) {
+        if (item != 0xffffffffu && !(item & kPreciseBit)) {
+            // a fast chunk, described by the producer (see fast_tag): its partial's index, whether
+            // it is a draft row's and whether it is the row's last chunk
+            const uint32_t fi = item & kFastIndexMask;
+            const bool is_draft = (item & kFastDraftBit) != 0;
+            check_ok(p.ws, (long long)fi < (long long)p.R.S * p.slots * p.cpr, -112, fi);
+            {
                 uint4 raw[kLoads];
 #pragma unroll
                 for (int v = 0; v < kLoads; ++v)
@@ -621,8 +628,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                 consume_all(raw);
                 __syncwarp();
                 if (lane == 0) mbar_arrive_relaxed(smem_u32(&empty[slot]));
-                if (chunk == p.cpr - 1) {  // the row's last chunk: mask past V
-                    const long long base = (long long)chunk * Geo<DT>::kChunk + lane * Geo<DT>::kPerVec;
+                if (item & kFastTailBit) {  // the row's last chunk: mask past V
+                    const long long base = (long long)(p.cpr - 1) * Geo<DT>::kChunk + lane * Geo<DT>::kPerVec;
 #pragma unroll
                     for (int v = 0; v < kLoads; ++v)
                         if (base + v * (Geo<DT>::kChunk / kLoads) >= p.R.V)
@@ -630,9 +637,19 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                                              : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
                 }
                 const float2 fp = fast_partial<DT>(raw, is_draft ? p.sc_d.c2 : p.sc_t.c2, p.ws);
-                if (lane == 0)
-                    ws_ptr<float2>(p.ws, p.L.fast)[((size_t)s * p.slots + rs) * p.cpr + chunk] = fp;
-            } else {
+                if (lane == 0) ws_ptr<float2>(p.ws, p.L.fast)[fi] = fp;
+            }
+            continue;
+        }
+        ChunkRef c{};
+        c.valid = false;
+        if (item != 0xffffffffu)
+            c = chunk_ref_two_list(p, item);
+        const int s = c.valid ? c.s : -1, rs = c.slot, chunk = c.chunk;
+        const bool sane = s < 0 || (check_ok(p.ws, chunk >= 0 && chunk < p.cpr, -111, chunk) &&
+                                    check_ok(p.ws, rs >= 0 && rs < p.slots, -112, rs));
+        if (s >= 0 && sane) {
+            {
                 // a sampled row: lane l takes the contiguous block of kSub logits at l * 128
                 // bytes, its pieces read with an XOR swizzle (piece v ^ (l & 7)) so that each
                 // quarter-warp touches eight different bank groups; the slot goes back when the
@@ -692,6 +709,7 @@ static cudaError_t launch_tma_t(const StreamParams& p0, cudaStream_t st) {
         p.div_fseq = make_fastdiv((uint32_t)(p.fslots > 0 ? p.fslots * p.cpr : 1));
         p.fper = sampled ? deal_fper(p.fslots) : p.fslots;
     }
+    if ((long long)p.R.S * p.slots * p.cpr > (long long)kFastIndexMask) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
