@@ -170,15 +170,17 @@ __device__ __forceinline__ bool check_ok(void*, bool, int, long long) { return t
 // warp collectives
 // ------------------------------------------------------------------------------------------
 
+// Warp maxima in one instruction each (redux.sync: integers since sm_80, floats since sm_100),
+// on every lane; a NaN lane is passed over, as fmaxf does.
 __device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
+    float r;
+    asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
 }
 __device__ __forceinline__ int warp_max_i(int v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
+    int r;
+    asm("redux.sync.max.s32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+    return r;
 }
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
