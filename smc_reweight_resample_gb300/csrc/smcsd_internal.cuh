@@ -62,12 +62,16 @@ __host__ __device__ inline int chunks_per_row(int V, int dtype) {
 
 // Geometry of the exp table of precise weights (bf16 logits): one entry per bf16 magnitude in
 // [2^-24, 64) for each sign, the positive ones at [0, kTabHalf), the negative ones at
-// [kTabStride, kTabStride + kTabHalf), each half followed by a zero entry.
+// [kTabStride, kTabStride + kTabHalf), each half followed by a zero entry (entries between the
+// halves, and one of padding at the end, are zero too). The negative half starts at entry 4096,
+// byte 32768 of the 8-byte entries: a logit's byte offset is its magnitude's times 8 with its
+// sign bit in bit 15, both halves of a 32-bit word of logits at once (tab_index2).
 constexpr uint32_t kTabMagLo = 0x3380u;                 // bf16 bits of 2^-24
 constexpr uint32_t kTabMagHi = 0x4280u;                 // bf16 bits of 64
 constexpr uint32_t kTabHalf = kTabMagHi - kTabMagLo;    // 3840 magnitudes per sign
-constexpr uint32_t kTabStride = kTabHalf + 1u;          // offset of the negative half
-constexpr int kTabSize = 2 * (int)kTabStride;           // 7682 entries, the two zero entries included
+constexpr uint32_t kTabStride = 4096u;                  // entry of the negative half's start
+constexpr int kTabSize = (int)(kTabStride + kTabHalf + 2u);  // 7938 entries (an even count)
+static_assert(kTabHalf * 8u < 32768u && kTabStride * 8u == 32768u, "exp table byte offsets");
 
 // ------------------------------------------------------------------------------------------
 // workspace layout

@@ -96,7 +96,7 @@ __device__ __forceinline__ void build_exp_table(float2* tab, const Scale& sc, co
     for (int i = tid; i < kTabSize; i += nthr) {
         const bool neg = i >= (int)kTabStride;
         const uint32_t m = (uint32_t)i - (neg ? kTabStride : 0u);
-        if (m == kTabHalf) {  // the zero entry after each half
+        if (m >= kTabHalf) {  // the zero entry after each half (and the unused entries)
             tab[i] = make_float2(0.0f, 0.0f);
             continue;
         }
@@ -116,7 +116,7 @@ __device__ __forceinline__ void build_exp_table(float2* tab, const Scale& sc, co
 // publishes it there (tag words: magic, then c_hi, c_lo, c2 bits); later calls with the same
 // scale copy it instead of rebuilding. A published table is never overwritten, so a reader can
 // never see a half-written one; calls with another scale build their own copy each time.
-constexpr uint32_t kTabMagic = 0x54424c32u;
+constexpr uint32_t kTabMagic = 0x54424c33u;
 __device__ __forceinline__ void setup_exp_table(float2* tab, const Scale& sc, const Exp2Table* T,
                                                 void* ws, uint32_t* gtag, float2* gtab, bool direct,
                                                 int tid, int nthr, int bar) {
@@ -468,15 +468,15 @@ struct RegSrc {
 // accumulator starts at 2^(nref+2) and stays below 2^(nref+8) <= 2^127.
 constexpr int kDirectMaxRef = 119;
 
-// Table indices of both bf16 logits of a word, as 16-bit halves: |z|'s offset from kTabMagLo
+// Table byte offsets of both bf16 logits of a word, as 16-bit halves: |z|'s offset from kTabMagLo
 // (taken modulo 2^16 without borrows between the halves) clamped to the zero entry kTabHalf,
-// plus kTabStride for a negative logit. `off` receives the unclamped offsets (a half >= kTabHalf:
-// outside the table's domain).
+// times 8, with the logit's sign bit kept in bit 15 (the negative half starts at byte 32768).
+// `off` receives the unclamped offsets (a half >= kTabHalf: outside the table's domain).
 __device__ __forceinline__ uint32_t tab_index2(uint32_t u, uint32_t& off) {
     off = ((u | 0x80008000u) - kTabMagLo * 0x10001u) ^ 0x80008000u;
     uint32_t c;
     asm("min.u16x2 %0, %1, %2;" : "=r"(c) : "r"(off), "r"(kTabHalf * 0x10001u));
-    return c + ((u >> 15) & 0x00010001u) * kTabStride;
+    return (c << 3) | (u & 0x80008000u);  // (c < 4096: no bit crosses into the other half)
 }
 
 // Table pass over a bf16 lane block: the sum of exp(c z) / 2^nref over the logits inside the
@@ -505,7 +505,7 @@ __device__ __forceinline__ dd table_pass(const Src& src, uint32_t tab, int nref,
             uint32_t off;
             const uint32_t ix = tab_index2(u, off);
             asm("max.u16x2 %0, %1, %2;" : "=r"(omax) : "r"(omax), "r"(off));
-            float2 e0 = lds_f2(tab + (ix & 0xffffu) * 8u), e1 = lds_f2(tab + (ix >> 16) * 8u);
+            float2 e0 = lds_f2(tab + (ix & 0xffffu)), e1 = lds_f2(tab + (ix >> 16));
             if (KIND == 2) {
                 const float s0 = pow2i(floor_int(f_mul(bf16_lo(u), c2)) - nref);
                 const float s1 = pow2i(floor_int(f_mul(bf16_hi(u), c2)) - nref);

@@ -344,8 +344,8 @@ __device__ __forceinline__ void pair_sums(const SharedSrc<DT>& src_t, const Shar
                 const uint32_t it = tab_index2(wt[j], ot), id = tab_index2(wd[j], od);
                 asm("max.u16x2 %0, %1, %2;" : "=r"(omax) : "r"(omax), "r"(ot));
                 asm("max.u16x2 %0, %1, %2;" : "=r"(omax) : "r"(omax), "r"(od));
-                const float2 et0 = lds_f2(tab + (it & 0xffffu) * 8u), et1 = lds_f2(tab + (it >> 16) * 8u);
-                const float2 ed0 = lds_f2(tab + (id & 0xffffu) * 8u), ed1 = lds_f2(tab + (id >> 16) * 8u);
+                const float2 et0 = lds_f2(tab + (it & 0xffffu)), et1 = lds_f2(tab + (it >> 16));
+                const float2 ed0 = lds_f2(tab + (id & 0xffffu)), ed1 = lds_f2(tab + (id >> 16));
                 acc_biased(t0, dd{et0.x, et0.y});
                 acc_biased(t1, dd{et1.x, et1.y});
                 acc_biased(d0, dd{ed0.x, ed0.y});
