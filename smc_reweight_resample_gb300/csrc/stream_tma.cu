@@ -353,10 +353,15 @@ __device__ __forceinline__ void pair_sums(const SharedSrc<DT>& src_t, const Shar
                 // p_i > q_i (a NaN difference, both masked, is not)
                 const bool c0 = f_sub(bf16_lo(wt[j]), bf16_lo(wd[j])) > theta;
                 const bool c1 = f_sub(bf16_hi(wt[j]), bf16_hi(wd[j])) > theta;
-                acc_biased(a0, c0 ? dd{et0.x, et0.y} : dd{0.0f, 0.0f});
-                acc_biased(b0, c0 ? dd{ed0.x, ed0.y} : dd{0.0f, 0.0f});
-                acc_biased(a1, c1 ? dd{et1.x, et1.y} : dd{0.0f, 0.0f});
-                acc_biased(b1, c1 ? dd{ed1.x, ed1.y} : dd{0.0f, 0.0f});
+                // (predicated additions: adding an exact zero would leave the same bits)
+                if (c0) {
+                    acc_biased(a0, dd{et0.x, et0.y});
+                    acc_biased(b0, dd{ed0.x, ed0.y});
+                }
+                if (c1) {
+                    acc_biased(a1, dd{et1.x, et1.y});
+                    acc_biased(b1, dd{ed1.x, ed1.y});
+                }
             }
             if ((omax & 0xffffu) >= kTabHalf || (omax >> 16) >= kTabHalf) pieces |= 1u << i;
             t0 = fast_two_sum(t0.hi, t0.lo);
