@@ -24,7 +24,7 @@
 
 namespace smcsd {
 
-constexpr int kSampleThreads = 256;  // three blocks per SM beside the 61 KB exp table
+constexpr int kSampleThreads = 256;  // three blocks per SM beside the 62 KB exp table
 
 template <int DT>
 struct ResidualBlock {
