@@ -272,7 +272,10 @@ static cudaError_t launch_finish_cluster_t(const StreamParams& p, cudaStream_t s
     const void* fn = reinterpret_cast<const void*>(kern);
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e == cudaSuccess && p.N > 8) e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return cudaErrorNotSupported;
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();  // (so that no later launch check reports this refusal)
+        return cudaErrorNotSupported;
+    }
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)p.R.S);
     cfg.blockDim = dim3((unsigned)(nw * kWarp));
