@@ -222,10 +222,13 @@ def test_smc_step_full_size(smcsd, cfg, steps):
     np.testing.assert_allclose(lw_gpu, lw_free, atol=FLOAT_ATOL, rtol=0)
 
 
-@pytest.mark.parametrize("GN", [(8, 16), (3, 48)], ids=["groups_of_16", "groups_of_48"])
+@pytest.mark.parametrize("GN", [(8, 16), (3, 48), (5, 2), (6, 5), (4, 12), (2, 24)],
+                         ids=["groups_of_16", "groups_of_48", "groups_of_2", "groups_of_5", "groups_of_12",
+                              "groups_of_24"])
 def test_fused_step_equals_separate_calls(smcsd, GN):
     """The fused step equals reweight + resample + remap called one by one; groups of 48 take
-    the fused step's path for groups larger than one warp."""
+    the fused step's path for groups larger than one warp, groups of 2..16 its thread-block
+    clusters (portable sizes up to 8, the opt-in size above), groups of 24 its arrival counter."""
     G, N = GN
     cfg = synth.SMCConfig("smc_small", G, N, 4, 20000, 3.0, 1.0, 1.0, 1.0, 256)
     S, K, V, G, N, P = cfg.S, cfg.K, cfg.V, cfg.G, cfg.N, cfg.pages_per_seq
